@@ -1,0 +1,618 @@
+#!/usr/bin/env python
+"""Benchmark of the OSCAR INT2 mixed-cache decode path on one GB300 (or N
+independent replicas, one per GPU).
+
+Headline (default workload ``qwen3_8b_32k_b1``): Qwen3-8B-shaped attention layer,
+batch 1, context 32768 = 4 BF16 sink + 32636 INT2 + 128 BF16 recent, 32 query /
+8 KV heads, head_dim 128.  One step = one decode step of one layer through the
+C ABI: oscar_quantize_append (the new token enters the BF16 window, the token
+leaving it is rotated/clipped/quantised into its INT2 page) followed by
+oscar_decode_attention (q R_K, split-K attention over INT2 + BF16 pages, LSE
+combine, o R_V^T).  Steps rotate over enough layer caches to exceed 3x the L2
+size, so every step reads its cache from HBM.  Inputs are synthetic (seeded
+generator); rotations come from the library's own calibration calls.
+
+metric = algorithmic bytes per step (INT2 codes + fp16 scale/zero + BF16 sink
+and window + q/out + append traffic) / step time, in GB/s.  Extra keys report
+the same-design BF16 kernel at the same batch, the roofline of the decode call,
+the fp64 oracle on the host (cpu_baseline) and an end-to-end number through the
+C ABI with host buffers.  ``--impl reference`` times the oracle alone.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from int2_rotated_kv_gb300 import pages, synth  # noqa: E402
+
+METRIC = "INT2 paged decode attn: HBM GB/s (% of ~8 TB/s), tokens/s vs own BF16 kernel"
+UNIT = "GB/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_split_qwen3_8b_32k.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
+    ap.add_argument("--workload", default=synth.QWEN3_8B_32K.name, choices=list(synth.WORKLOADS))
+    ap.add_argument("--extras", action="store_true", help="also time the 128k, prefix and budget configs")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-calib", type=int, default=None)
+    ap.add_argument("--profile", action="store_true",
+                    help="minimal run for ncu: one layer cache, eager steps, no extra legs")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- util
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler running while the timed region runs."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[6:10]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "layout.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "int2_rotated_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------- byte accounting
+
+def token_bytes(d):
+    return 3 * d // 4, 4 * d          # INT2 token-head (K+V codes + fp16 s/z), BF16 token-head
+
+
+def attention_bytes(lens, hkv, hq, d, sink, window, bf16_only=False):
+    i2, bf = token_bytes(d)
+    tot = 0
+    for L in lens:
+        L = int(L)
+        if bf16_only:
+            tot += hkv * L * bf
+        else:
+            n_int2 = max(0, L - window - sink)
+            tot += hkv * (n_int2 * i2 + (L - n_int2) * bf)
+    tot += 2 * len(lens) * hq * d * 2          # q read, out written (bf16)
+    return tot
+
+
+def append_bytes(lens, hkv, d, sink, window, bf16_only=False):
+    i2, bf = token_bytes(d)
+    tot = 0
+    for L in lens:
+        tot += hkv * (bf + bf)                  # read new token, write it to its BF16 slot
+        if not bf16_only and int(L) - 1 - window >= sink:
+            tot += hkv * (bf + i2)              # read the leaving token, write its INT2 form
+    return tot
+
+
+# ----------------------------------------------------------------- setup
+
+def calibrate_with_library(inst, n_calib):
+    """R_K, R_V and clips per KV head through the library's host calls."""
+    from int2_rotated_kv_gb300 import _lib as L
+    rk, rv, ck, cv = [], [], [], []
+    for h in range(inst.workload.num_kv_heads):
+        q = inst.calib_q[h][:n_calib]
+        k = inst.calib_k[h][:n_calib]
+        v = inst.calib_v[h][:n_calib]
+        cq = L.oscar_query_covariance(q)
+        cs = L.oscar_score_covariance(q, k, v, 0)
+        _, r_k, c_k, _ = L.oscar_build_rotation(cq, k, 99.9, L.VARIANT_OSCAR)
+        _, r_v, c_v, _ = L.oscar_build_rotation(cs, v, 99.9, L.VARIANT_OSCAR)
+        rk.append(r_k); rv.append(r_v); ck.append(c_k); cv.append(c_v)
+    return np.stack(rk), np.stack(rv), np.array(ck, np.float32), np.array(cv, np.float32)
+
+
+def bf16_dev(a, dev):
+    import torch
+    return torch.from_numpy(synth.bf16_bits(np.asarray(a, np.float32)).view(np.int16).copy()).view(
+        torch.bfloat16).to(dev)
+
+
+def prefill_layer(cache, inst, lens, dev):
+    import torch
+    from int2_rotated_kv_gb300 import _lib as L
+    H = inst.workload.num_kv_heads
+    ks, vs, sid, pos = [], [], [], []
+    for b, n in enumerate(lens):
+        n = int(n)
+        ks.append(np.stack([inst.k[b][h][:n] for h in range(H)], 1))
+        vs.append(np.stack([inst.v[b][h][:n] for h in range(H)], 1))
+        sid.append(np.full(n, b, np.int32))
+        pos.append(np.arange(n, dtype=np.int32))
+    L.oscar_prefill_quantize(cache, bf16_dev(np.concatenate(ks), dev), bf16_dev(np.concatenate(vs), dev),
+                             torch.from_numpy(np.concatenate(sid)).to(dev),
+                             torch.from_numpy(np.concatenate(pos)).to(dev),
+                             torch.tensor(np.asarray(lens, np.int32), device=dev))
+    torch.cuda.synchronize()
+
+
+def clone_cache(c):
+    import dataclasses
+    return dataclasses.replace(c, int2_pool=c.int2_pool.clone(), bf16_pool=c.bf16_pool.clone())
+
+
+class Decoder:
+    """One set of layer caches plus the per-step calls (INT2 mixed or BF16-only)."""
+
+    def __init__(self, inst, lens_final, rot, dev, *, bf16_only=False, l2_bytes=0):
+        import torch
+        from int2_rotated_kv_gb300 import _lib as L
+        w = inst.workload
+        self.L, self.torch, self.dev = L, torch, dev
+        self.w, self.bf16_only = w, bf16_only
+        self.S = w.sink
+        self.W = max(int(lens_final.max()) + 1, 1) if bf16_only else w.window
+        if bf16_only:
+            self.S = 0
+        self.lens = np.asarray(lens_final, np.int64)
+        B, hkv, hq, d = len(self.lens), w.num_kv_heads, w.num_q_heads, w.head_dim
+        # the cache is filled up to L-1; every step re-plays the decode step to L
+        pp = pages.plan(self.lens - 1, self.S, self.W, growth=1,
+                        shared_prefix_tokens=w.shared_prefix)
+        rk, rv, ck, cv = rot
+        base = pages.allocate(pp, hkv=hkv, hq=hq, d=d, sink=self.S, window=self.W, device=dev,
+                              r_k=rk, r_v=rv, clip_k=ck, clip_v=cv)
+        prefill_layer(base, inst, self.lens - 1, dev)
+        self.layer_bytes = (base.int2_pool.numel() + base.bf16_pool.numel() * 2)
+        self.step_bytes = attention_bytes(self.lens, hkv, hq, d, self.S, self.W, bf16_only)
+        self.attn_bytes = self.step_bytes
+        self.step_bytes += append_bytes(self.lens, hkv, d, self.S, self.W, bf16_only)
+        touched = attention_bytes(self.lens, hkv, hq, d, self.S, self.W, bf16_only)
+        n_layers = max(2, math.ceil(3 * l2_bytes / max(touched, 1)) + 1) if l2_bytes else 1
+        self.caches = [base] + [clone_cache(base) for _ in range(n_layers - 1)]
+        kn = np.stack([[inst.k[b][h][int(self.lens[b]) - 1] for h in range(hkv)] for b in range(B)])
+        vn = np.stack([[inst.v[b][h][int(self.lens[b]) - 1] for h in range(hkv)] for b in range(B)])
+        self.k_new, self.v_new = bf16_dev(kn, dev), bf16_dev(vn, dev)
+        self.q = bf16_dev(inst.q, dev)
+        self.lens_dev = torch.tensor(self.lens.astype(np.int32), device=dev)
+        self.max_len = int(self.lens.max())
+        self.out = torch.zeros((B, hq, d), dtype=torch.bfloat16, device=dev)
+        ws = L.oscar_decode_workspace_size(base, B, self.max_len)
+        self.ws = torch.empty(ws // 4 + 64, dtype=torch.float32, device=dev)
+        self.n_layers = n_layers
+        self.launches_per_step = 4 if not bf16_only else 3
+
+    def append(self, i, k=None, v=None, lens=None):
+        c = self.caches[i % self.n_layers]
+        self.L.oscar_quantize_append(c, self.k_new if k is None else k, self.v_new if v is None else v,
+                                     self.lens_dev if lens is None else lens)
+
+    def attend(self, i, q=None, lens=None, out=None):
+        c = self.caches[i % self.n_layers]
+        fn = self.L.oscar_decode_attention_bf16 if self.bf16_only else self.L.oscar_decode_attention
+        fn(c, self.q if q is None else q, self.lens_dev if lens is None else lens, self.max_len,
+           self.out if out is None else out, self.ws)
+
+    def step(self, i):
+        self.append(i)
+        self.attend(i)
+
+    def graph(self, first, count):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(first, first + count):     # populate allocator / attributes
+                self.step(i)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(first, first + count):
+                self.step(i)
+        return g
+
+
+def time_steps(dec, steps, warmup, chunk=64, clocks=None, barrier=None):
+    """Time exactly `steps` decode steps (graph replays), after `warmup` steps."""
+    torch = dec.torch
+    chunk = max(dec.n_layers, (chunk // dec.n_layers) * dec.n_layers)
+    g_full = dec.graph(0, chunk)
+    rem = steps % chunk
+    g_rem = dec.graph(0, rem) if rem else None
+    for i in range(warmup):
+        dec.step(i)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    if clocks:
+        clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(steps // chunk):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1) / steps, clk
+
+
+def time_decode_calls(dec, iters=200, batch=40):
+    """Average duration of one oscar_decode_attention call (its three kernels),
+    bracketed by CUDA events on the launching stream, cold L2 (rotating layers).
+    A spin kernel keeps the stream busy while a batch of calls is queued, so the
+    host's launch cost never shows up between the events."""
+    torch = dec.torch
+    for i in range(10):
+        dec.attend(i)
+    torch.cuda.synchronize()
+    ts = []
+    done = 0
+    while done < iters:
+        n = min(batch, iters - done)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        torch.cuda._sleep(20_000_000)
+        for k, (a, b) in enumerate(evs):
+            a.record()
+            dec.attend(done + k)
+            b.record()
+        torch.cuda.synchronize()
+        ts += [a.elapsed_time(b) for a, b in evs]
+        done += n
+    return statistics.median(ts), statistics.mean(ts)
+
+
+def time_e2e(dec, steps, warmup):
+    """Through the C ABI with host buffers: per step copy q and the new K/V from
+    pinned host memory, append + attend, copy the output back."""
+    torch = dec.torch
+    hq = torch.empty(dec.q.shape, dtype=torch.bfloat16).pin_memory()
+    hk = torch.empty(dec.k_new.shape, dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty(dec.v_new.shape, dtype=torch.bfloat16).pin_memory()
+    hq.copy_(dec.q.cpu()); hk.copy_(dec.k_new.cpu()); hv.copy_(dec.v_new.cpu())
+    ho = torch.empty(dec.out.shape, dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv, do = (torch.empty_like(dec.q), torch.empty_like(dec.k_new),
+                      torch.empty_like(dec.v_new), torch.empty_like(dec.out))
+
+    def one(i):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dec.append(i, dk, dv)
+        dec.attend(i, dq, out=do)
+        ho.copy_(do, non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    return e0.elapsed_time(e1) / steps, h2d, ho.numel() * 2
+
+
+# -------------------------------------------------------------- CPU / oracle
+
+def oracle_sample(inst, rot, n_heads=1, max_tokens=None):
+    """The oracle's decode for the first `n_heads` KV heads of sequence 0 (its
+    INT2 tokens rebuilt and attended in fp64).  Returns (bytes, seconds)."""
+    from oracle import attention, cache as ocache
+    w = inst.workload
+    rk, rv, ck, cv = rot
+    L = int(inst.seq_lens[0]) if max_tokens is None else min(int(inst.seq_lens[0]), max_tokens)
+    G = w.gqa
+    t0 = time.perf_counter()
+    for h in range(n_heads):
+        r = ocache.Rotations([rk[h]], [rv[h]], [ck[h]], [cv[h]])
+        attention.mixed_decode(inst.q[:1, h * G:(h + 1) * G], [[inst.k[0][h][:L]]],
+                               [[inst.v[0][h][:L]]], [L], r, sink=w.sink, window=w.window, gqa=G)
+    dt = time.perf_counter() - t0
+    nb = attention_bytes([L], n_heads, n_heads * G, w.head_dim, w.sink, w.window)
+    return nb, dt
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        n = max((i.get("num_threads", 1) for i in info), default=os.cpu_count())
+        return int(n)
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(inst, rot, budget_s=12.0):
+    nb, dt = oracle_sample(inst, rot, 1)
+    heads = 1
+    tot_b, tot_t = nb, dt
+    while tot_t < budget_s and heads < inst.workload.num_kv_heads:
+        b2, t2 = oracle_sample(inst, rot, 1)
+        tot_b += b2
+        tot_t += t2
+        heads += 1
+    return {"value": round(tot_b / tot_t / 1e9, 4), "unit": UNIT, "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle decode of {heads} KV-head pass(es) (G={inst.workload.gqa} "
+                      f"query heads, full {int(inst.seq_lens[0])}-token context) of the step; "
+                      f"{tot_t:.1f} s of CPU work"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    inst = synth.draw_instance(w, n_calib=min(w.n_calib, 1024))
+    from oracle import attention
+    rot_o = attention.calibrate(inst.calib_q, inst.calib_k, inst.calib_v, 0)
+    rot = (np.stack(rot_o.rk), np.stack(rot_o.rv), np.array(rot_o.ck), np.array(rot_o.cv))
+    # size the per-step sample so the whole run stays within ~2 minutes
+    nb, dt = oracle_sample(inst, rot, 1, max_tokens=2048)
+    per_tok = dt / 2048
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    ntok = int(min(int(inst.seq_lens[0]), max(w.window + w.sink + 16, budget / per_tok)))
+    for _ in range(args.warmup):
+        oracle_sample(inst, rot, 1, max_tokens=ntok)
+    tb = tt = 0.0
+    for _ in range(args.steps):
+        b, t = oracle_sample(inst, rot, 1, max_tokens=ntok)
+        tb += b
+        tt += t
+    v = tb / tt / 1e9
+    sample = (f"fp64 numpy oracle, 1 KV head (G={w.gqa}) of sequence 0, first {ntok} tokens "
+              f"of the context per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample_tokens": ntok},
+        "cpu_baseline": {"value": round(v, 5), "unit": UNIT, "kind": "oracle",
+                         "cores": blas_threads(), "sample": sample},
+        "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------- extras
+
+def extra_decode(name, dev, l2, n_calib, steps=200, warmup=10):
+    """µs/layer and GB/s for another workload (INT2 and BF16 at the same batch)."""
+    torch = __import__("torch")
+    w = synth.WORKLOADS[name]
+    inst = synth.draw_instance(w, n_calib=n_calib)
+    rot = calibrate_with_library(inst, n_calib)
+    dec = Decoder(inst, inst.seq_lens, rot, dev, l2_bytes=l2)
+    t, _ = time_steps(dec, steps, warmup)
+    med, _ = time_decode_calls(dec, 100)
+    res = {"us_per_layer_step": round(t * 1e3, 3), "GBps": round(dec.step_bytes / t / 1e6, 1),
+           "decode_call_us": round(med * 1e3, 3),
+           "decode_call_GBps": round(dec.attn_bytes / med / 1e6, 1),
+           "batch": len(inst.seq_lens), "layers_rotated": dec.n_layers}
+    del dec
+    torch.cuda.empty_cache()
+    try:
+        decb = Decoder(inst, inst.seq_lens, rot, dev, bf16_only=True, l2_bytes=l2)
+        tb, _ = time_steps(decb, steps, warmup)
+        res["bf16_us_per_layer_step"] = round(tb * 1e3, 3)
+        res["bf16_GBps"] = round(decb.step_bytes / tb / 1e6, 1)
+        res["speedup_vs_bf16"] = round(tb / t, 3)
+        del decb
+    except Exception as e:   # out of memory for the BF16 copy of a very long context
+        res["bf16_error"] = str(e)[:120]
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+
+        def barrier():
+            dist.barrier()
+    from int2_rotated_kv_gb300 import _lib as L
+    L.lib()
+    w = synth.WORKLOADS[args.workload]
+    n_calib = args.n_calib or w.n_calib
+    t0 = time.time()
+    inst = synth.draw_instance(w, n_calib=n_calib)
+    t_gen = time.time() - t0
+    t0 = time.time()
+    rot = calibrate_with_library(inst, n_calib)
+    t_cal = time.time() - t0
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    if args.profile:
+        # launches in order: 1 prefill, then per step append, qrot, split, combine
+        dec = Decoder(inst, inst.seq_lens, rot, dev, l2_bytes=0)
+        for i in range(args.warmup + args.steps):
+            dec.step(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": w.name, "steps": args.steps, "warmup": args.warmup,
+                          "launches_per_step": dec.launches_per_step,
+                          "attention_bytes": int(dec.attn_bytes)}), flush=True)
+        return
+    dec = Decoder(inst, inst.seq_lens, rot, dev, l2_bytes=l2)
+    clocks = Clocks(local)
+    ms, clk = time_steps(dec, args.steps, args.warmup, clocks=clocks, barrier=barrier)
+    ms_all = ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_all = float(t.item())
+    value = world * dec.step_bytes / (ms_all * 1e-3) / 1e9
+    # roofline of the decode call (qrot + split + combine), cold L2
+    med, mean = time_decode_calls(dec, 200)
+    peak, peak_kind = peaks()
+    achieved = dec.attn_bytes / (mean * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            prof = json.load(f)
+        if prof.get("source_hash") == kernel_source_hash() and prof.get("workload") == w.name:
+            traffic = prof.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    # end to end through the C ABI with host buffers
+    e2e_ms, h2d, d2h = time_e2e(dec, min(args.steps, 500), max(3, args.warmup))
+    e2e_val = world * dec.step_bytes / (e2e_ms * 1e-3) / 1e9
+    # same-design BF16 kernel, same batch
+    bf = {}
+    try:
+        decb = Decoder(inst, inst.seq_lens, rot, dev, bf16_only=True, l2_bytes=l2)
+        msb, _ = time_steps(decb, min(args.steps, 1000), args.warmup)
+        medb, meanb = time_decode_calls(decb, 100)
+        bf = {"bf16_ms_per_step": round(msb, 5), "bf16_GBps": round(decb.step_bytes / msb / 1e6, 1),
+              "bf16_decode_call_us": round(meanb * 1e3, 3),
+              "bf16_decode_call_GBps": round(decb.attn_bytes / meanb / 1e6, 1),
+              "speedup_vs_bf16": round(msb / ms, 3),
+              "bf16_cache_bytes_per_layer": int(decb.attn_bytes)}
+        del decb
+        torch.cuda.empty_cache()
+    except Exception as e:
+        bf = {"bf16_error": str(e)[:200]}
+    B = len(inst.seq_lens)
+    layers_model = w.layers if w.layers > 1 else 1
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_all, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int2+bf16/f32acc",
+        "data": "synthetic (seeded generator; rotations from the library's calibration calls)",
+        "config": {"workload": w.name, "batch": B, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "context": int(inst.seq_lens.max()), "sink": w.sink, "window": w.window,
+                   "n_calib": n_calib, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: steps rotate over {dec.n_layers} layer caches "
+                         f"({dec.n_layers * dec.attn_bytes / 1e6:.0f} MB touched vs L2 {l2 / 1e6:.0f} MB)",
+                   "step": "oscar_quantize_append + oscar_decode_attention, one layer, CUDA graph"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "oscar_decode_attention call (qrot + split + combine kernels)",
+                     "peak_kind": f"{peak_kind} hbm_gbs", "call_us_median": round(med * 1e3, 3),
+                     "call_us_mean": round(mean * 1e3, 3),
+                     "algorithmic_bytes_per_call": int(dec.attn_bytes)},
+        "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": dec.launches_per_step * args.steps,
+        "clocks": clk,
+        "us_per_layer_step": round(ms_all * 1e3, 3),
+        "decode_tokens_per_s_attention_only": round(world * B / (layers_model * ms_all * 1e-3), 1),
+        "tokens_per_s_layers": layers_model,
+        "algorithmic_bytes_per_step": int(dec.step_bytes),
+        "setup_s": {"generate": round(t_gen, 1), "calibrate": round(t_cal, 1)},
+    }
+    out.update(bf)
+    if args.extras and rank == 0:
+        ex = {}
+        for name in (synth.QWEN3_32B_128K.name,):
+            try:
+                ex[name] = extra_decode(name, dev, l2, 2048)
+            except Exception as e:
+                ex[name] = {"error": str(e)[:200]}
+        out["extras"] = ex
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(inst, rot)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * oscar.h -- C ABI of the OSCAR mixed-precision INT2 KV-cache library (sm_103a).
+ *
+ * The library implements the online serving path of OSCAR (Offline Spectral
+ * Covariance-Aware Rotation for 2-bit KV cache quantisation) and the offline
+ * rotation builder that feeds it.  Sources, cited by page and section:
+ *   [Summary]  "Technical Summary: OSCAR - Offline Spectral Covariance-Aware
+ *              Rotation for 2-bit KV Cache Quantization" (gist.science);
+ *   [Abstract] the arXiv abstract on the page "OSCAR: Offline Spectral
+ *              Covariance-Aware Rotation for 2-bit KV Cache Quantization".
+ *
+ * Conventions shared by every call
+ *   - Activations are row vectors; a rotation acts on the right: y = x R.
+ *   - Pointers documented "device" must be device memory of the current CUDA
+ *     device; "host" pointers are ordinary host memory.  All memory is owned
+ *     by the caller; the library never allocates device memory, never frees
+ *     anything and never synchronises a stream.
+ *   - Argument errors are detected on the host and returned before any kernel
+ *     is launched.  A launch failure returns OSCAR_ERR_CUDA (cudaGetLastError).
+ *     Faults found inside kernels (an out-of-range page id, a wait that ran out
+ *     of time) are never trapped: the kernel skips the bad access and ORs a bit
+ *     into the optional device word desc->status (see OSCAR_DEVERR_*).
+ *   - `stream` is a cudaStream_t passed as void*; 0 means the legacy stream.
+ *   - Calls are stateless and may be issued from several host threads.
+ *
+ * Cache format (one layer).  Page size 16 tokens, quantisation group 32
+ * channels, head_dim d in {64, 128}, G = num_q_heads / num_kv_heads in
+ * {1, 2, 4, 8}.  A sequence of length L (current token included) keeps tokens
+ * t < sink and t >= L - window in BF16 pages, and tokens sink <= t < L - window
+ * in INT2 pages [Summary 2.2B, "Mixed-Precision Layout"].  Logical page
+ * p = t / 16 of sequence b maps to a physical page through two tables of int32
+ * ids, int2_page_table[b * max_pages_per_seq + p] and bf16_page_table[...]
+ * (-1 = none); equal ids in several rows share a page (prefix caching,
+ * [Summary 2.2B "Kernel Integration"], [Summary 3.3]).
+ *   INT2 pool: num_int2_pages * num_kv_heads blocks of 12*d bytes; block
+ *     (page, head) at byte (page*num_kv_heads + head)*12*d holds, for the 16
+ *     slots, key codes (4d B), key fp16 (scale, zero) pairs (2d B), value codes
+ *     (4d B), value fp16 scales (d B) and zeros (d B), in the fragment order
+ *     documented in int2_rotated_kv_gb300/csrc/layout.cuh.
+ *   BF16 pool: num_bf16_pages * num_kv_heads blocks of 64*d bytes (keys then
+ *     values, 16*d bf16 each, same fragment order).
+ * Stored INT2 values are, per group of 32 rotated channels, code*s + z with
+ * s = fp16((max-min)/3), z = fp16(min) of the clipped group and
+ * code = round-half-even((y_clipped - z)/s) in [0, 3] (0 when s == 0).
+ */
+#ifndef OSCAR_H_
+#define OSCAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int oscar_status;
+#define OSCAR_OK 0
+#define OSCAR_ERR_INVALID_ARG (-1)   /* null pointer, negative size, bad combination   */
+#define OSCAR_ERR_UNSUPPORTED (-2)   /* shape outside the supported set                 */
+#define OSCAR_ERR_WORKSPACE (-3)     /* workspace too small                             */
+#define OSCAR_ERR_CUDA (-4)          /* a CUDA runtime call or a launch failed          */
+#define OSCAR_ERR_NOT_CONVERGED (-5) /* eigen-solver did not converge / degenerate gap  */
+
+/* bits ORed into *desc->status by kernels (never trapped) */
+#define OSCAR_DEVERR_PAGE_ID 1       /* a page id outside [0, num_pages) was skipped    */
+#define OSCAR_DEVERR_TIMEOUT 2       /* an mbarrier wait ran out of time                */
+#define OSCAR_DEVERR_SEQ_LEN 4       /* a length or position outside its valid range    */
+
+#define OSCAR_VARIANT_OSCAR 0        /* R = U H P_br                                    */
+#define OSCAR_VARIANT_HADAMARD 1     /* R = H (data-oblivious baseline)                 */
+#define OSCAR_VARIANT_IDENTITY 2     /* R = I (unrotated baseline)                      */
+
+typedef struct oscar_cache_desc {
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  int32_t head_dim;                /* 64 or 128                                       */
+  int32_t sink;                    /* BF16 tokens at the start (>= 0)                 */
+  int32_t window;                  /* BF16 recent tokens (>= 1)                       */
+  int32_t max_pages_per_seq;       /* row length of both page tables                  */
+  int64_t num_int2_pages;          /* physical pages in the INT2 pool                 */
+  int64_t num_bf16_pages;          /* physical pages in the BF16 pool                 */
+  void* int2_pool;                 /* device, see format above                        */
+  void* bf16_pool;                 /* device                                          */
+  const int32_t* int2_page_table;  /* device [batch][max_pages_per_seq]               */
+  const int32_t* bf16_page_table;  /* device [batch][max_pages_per_seq]               */
+  const float* r_k;                /* device [num_kv_heads][d][d], y = x R_K, 16-B aligned */
+  const float* r_v;                /* device [num_kv_heads][d][d], 16-byte aligned    */
+  const float* clip_k;             /* device [num_kv_heads]                           */
+  const float* clip_v;             /* device [num_kv_heads]                           */
+  int32_t* status;                 /* optional device word (OSCAR_DEVERR_* bits)      */
+} oscar_cache_desc;
+
+/* ---------------------------------------------------------------- host calls */
+
+/* Query-aware key target C_Q = (1/N) sum_n q_n^T q_n [Summary 2.1, 2.2A.1].
+ * q: host fp32 [n][g][d] calibration queries of the g query heads that read one
+ * KV head (pooled: the sum runs over n and g, normaliser n*g).
+ * c_out: host fp64 [d][d].  Synchronous, no CUDA. */
+oscar_status oscar_query_covariance(int32_t d, int32_t g, int64_t n, const float* q,
+                                    double* c_out);
+
+/* Score-aware value target C_S = (1/N) V^T S^T S V [Summary 2.1, 2.2A.1], with S
+ * the post-softmax causal attention probabilities (scale 1/sqrt(d)) of each of
+ * the g query heads over one calibration sequence: C_S = (1/(n g)) sum_h
+ * (S_h V)^T (S_h V).  q: host fp32 [n][g][d]; k, v: host fp32 [n][d].
+ * d must be a multiple of 4.  num_threads <= 0 uses every hardware thread.
+ * c_out: host fp64 [d][d]. */
+oscar_status oscar_score_covariance(int32_t d, int32_t g, int64_t n, const float* q,
+                                    const float* k, const float* v, int32_t num_threads,
+                                    double* c_out);
+
+/* Offline rotation and clip for one (layer, KV head, K or V) [Summary 2.2A.2-4]:
+ * eigen-decompose C (Jacobi, fp64), order eigenvectors by descending eigenvalue,
+ * make the largest-magnitude entry of each column positive (ties: lowest row),
+ * form R = U H P_br (H the normalised Sylvester Hadamard, P_br[i][br(i)] = 1),
+ * round R to fp32, and set clip = the `percentile` (linear interpolation between
+ * order statistics) of |calib_x R32| over all n*d entries.
+ * variant: OSCAR_VARIANT_* (HADAMARD and IDENTITY ignore c).
+ * c: host fp64 [d][d] symmetric; calib_x: host fp32 [n][d]; n >= 1.
+ * Outputs (host): r64_out [d][d] (nullable), r32_out [d][d], clip_out [1],
+ * eigvals_out [d] (nullable).  d must be a power of two in [2, 256].
+ * Returns OSCAR_ERR_NOT_CONVERGED if the sweep limit is hit or two eigenvalues
+ * are closer than 1e-12 * ||C|| (the eigenbasis would not be unique). */
+oscar_status oscar_build_rotation(int32_t d, const double* c, const float* calib_x, int64_t n,
+                                  double percentile, int32_t variant, double* r64_out,
+                                  float* r32_out, float* clip_out, double* eigvals_out);
+
+/* ------------------------------------------------------------- device calls */
+
+/* Bulk placement of prompt tokens [Summary 2.2B]: every token i of the list
+ * (sequence seq_ids[i], position positions[i]) is written either to its BF16
+ * slot (when it is a sink or recent token for the sequence's final length
+ * seq_lens_final[seq]) or rotated by R_K / R_V, clipped, quantised and packed
+ * into its INT2 slot.  k, v: device bf16 [total_tokens][num_kv_heads][d];
+ * seq_ids, positions: device int32 [total_tokens]; seq_lens_final: device int32
+ * [num_seqs], indexed by sequence id (ids must lie in [0, num_seqs) and index
+ * rows of the page tables).  Tokens sharing a page are fine; two tokens with
+ * the same (sequence, position) race.  Asynchronous on `stream`. */
+oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k, const void* v,
+                                    const int32_t* seq_ids, const int32_t* positions,
+                                    const int32_t* seq_lens_final, int32_t num_seqs,
+                                    int64_t total_tokens, void* stream);
+
+/* One decode step of cache maintenance for `batch` sequences [Summary 2.2B]:
+ * sequence b's new token (position L-1, L = seq_lens_after[b]) is written to its
+ * BF16 slot, and when L > sink + window the token at position L-1-window, which
+ * has just left the recent window, is read from its BF16 slot, rotated, clipped,
+ * quantised and packed into its INT2 slot.  k_new, v_new: device bf16
+ * [batch][num_kv_heads][d]; seq_lens_after: device int32 [batch].  The caller
+ * allocates the pages beforehand.  Asynchronous. */
+oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_new,
+                                   const void* v_new, const int32_t* seq_lens_after,
+                                   int32_t batch, void* stream);
+
+/* Bytes of device workspace oscar_decode_attention / _bf16 need for this batch
+ * and maximum sequence length (depends on the device's SM count). */
+size_t oscar_decode_workspace_size(const oscar_cache_desc* desc, int32_t batch,
+                                   int32_t max_seq_len);
+
+/* Decode attention over the mixed cache [Summary 2.2B "Kernel Integration"],
+ * [Abstract]: out[b][hq] = softmax(q k~^T / sqrt(d)) v~ over the L = seq_lens[b]
+ * tokens of sequence b, where query head hq reads KV head hq / G, BF16 tokens
+ * are used as stored and INT2 tokens stand for k~ = y_hat_K R_K^T,
+ * v~ = y_hat_V R_V^T.  The kernel never forms k~ or v~: it rotates the query
+ * once (q R_K), attends in the rotated basis, and rotates the INT2 part of the
+ * output back once (o R_V^T); split-K partials are merged with log-sum-exp.
+ * q, out: device bf16 [batch][num_q_heads][d]; seq_lens: device int32 [batch]
+ * (each in [1, max_seq_len], max_seq_len <= 16 * max_pages_per_seq);
+ * workspace: device, >= oscar_decode_workspace_size bytes, 16-byte aligned,
+ * no initial contents required.  Asynchronous. */
+oscar_status oscar_decode_attention(const oscar_cache_desc* desc, const void* q,
+                                    const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/* Same-design BF16 baseline [Summary 4, the BF16 comparison]: every token of
+ * every sequence is read from the BF16 pool through bf16_page_table; the INT2
+ * fields of desc are ignored.  Arguments as oscar_decode_attention. */
+oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const void* q,
+                                         const int32_t* seq_lens, int32_t batch,
+                                         int32_t max_seq_len, void* out, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/* Number of SMs the split heuristics assume for the current device (>= 1). */
+int32_t oscar_device_sm_count(void);
+
+/* Static text for a status code. */
+const char* oscar_status_string(oscar_status s);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t oscar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H_ */

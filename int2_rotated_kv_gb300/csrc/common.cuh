@@ -1,0 +1,186 @@
+// Device helpers shared by the kernels: inline PTX for warp-level MMA, matrix
+// transpose, mbarriers, bulk (TMA) copies and programmatic dependent launch.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "oscar.h"
+
+namespace oscar {
+
+constexpr int kPage = 16;
+constexpr int kGroup = 32;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// D += A * B, m16n8k16, f16 inputs, f32 accumulate (PTX ISA "mma.sync").
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 b16 matrix held one row-pair per lane (PTX "movmatrix").
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+
+__device__ __forceinline__ float bf16_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarriers
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~2 s, records OSCAR_DEVERR_TIMEOUT and returns
+// false instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > 2000000000ull) {
+      if (status) atomicOr(status, OSCAR_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bulk global -> shared copy (TMA, non-tensor), completion on an mbarrier.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------ programmatic dependent launch
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace oscar
+
+// ------------------------------------------------------------ host helpers
+
+namespace oscar_host {
+
+inline bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+// Checks shared by the device calls.  needs_int2: INT2 fields must be valid.
+inline oscar_status check_desc(const oscar_cache_desc* c, bool needs_int2, bool needs_bf16) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (c->num_kv_heads < 1 || c->num_q_heads < 1 || c->sink < 0 || c->window < 1 ||
+      c->max_pages_per_seq < 1)
+    return OSCAR_ERR_INVALID_ARG;
+  if (!head_dim_ok(c->head_dim)) return OSCAR_ERR_UNSUPPORTED;
+  if (c->num_q_heads % c->num_kv_heads) return OSCAR_ERR_INVALID_ARG;
+  const int g = c->num_q_heads / c->num_kv_heads;
+  if (!(g == 1 || g == 2 || g == 4 || g == 8)) return OSCAR_ERR_UNSUPPORTED;
+  if (needs_bf16 && (!c->bf16_pool || !c->bf16_page_table || c->num_bf16_pages < 1))
+    return OSCAR_ERR_INVALID_ARG;
+  if (needs_int2 && (!c->int2_pool || !c->int2_page_table || c->num_int2_pages < 1 || !c->r_k ||
+                     !c->r_v || !c->clip_k || !c->clip_v))
+    return OSCAR_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(c->int2_pool) | reinterpret_cast<uintptr_t>(c->bf16_pool)) & 15)
+    return OSCAR_ERR_INVALID_ARG;
+  if (needs_int2 && ((reinterpret_cast<uintptr_t>(c->r_k) | reinterpret_cast<uintptr_t>(c->r_v)) & 15))
+    return OSCAR_ERR_INVALID_ARG;   // rotations are staged by 16-byte bulk copies
+  return OSCAR_OK;
+}
+
+int sm_count();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (function, device).
+bool allow_smem(const void* func, int bytes);
+
+}  // namespace oscar_host

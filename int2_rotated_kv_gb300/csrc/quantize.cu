@@ -1,0 +1,389 @@
+// Rotate + clip + INT2-quantise + pack: moves tokens into the mixed cache.
+//
+// "Technical Summary: OSCAR ...", section 2.2B: the middle history is stored
+// in INT2 after the fixed rotation and clipping; sink and recent tokens stay
+// BF16.  One kernel serves both entry points:
+//   prefill: a list of (sequence, position) tokens with their bf16 K/V; each is
+//            copied to its BF16 slot or quantised into its INT2 slot;
+//   append:  per sequence, the new token goes to its BF16 slot and the token
+//            that just left the recent window is read back from its BF16 slot
+//            and quantised into its INT2 slot.
+// A CTA owns one (KV head, K-or-V) pair, keeps that head's d x d rotation in
+// shared memory and walks tiles of 32 tokens: y = x R with fp32 FMAs in index
+// order, then per group of 32 channels (one warp, one lane per channel) clip,
+// min/max, s16 = fp16((max-min)/3), z16 = fp16(min), code =
+// rint((y_c - z16)/s16) clamped to [0,3], each step rounded in fp32 exactly as
+// written, then the codes are packed byte by byte into the page format of
+// layout.cuh (every byte holds codes of one token, so slots never collide).
+#include <algorithm>
+
+#include "common.cuh"
+#include "layout.cuh"
+
+namespace oscar {
+
+constexpr int kQTile = 32;
+constexpr int kQThreads = 256;
+
+struct QuantParams {
+  int hkv, sink, window, max_pages;
+  int64_t n_int2_pages, n_bf16_pages;
+  uint8_t* int2_pool;
+  uint16_t* bf16_pool;
+  const int32_t* int2_pt;
+  const int32_t* bf16_pt;
+  const float* r_k;
+  const float* r_v;
+  const float* clip_k;
+  const float* clip_v;
+  int32_t* status;
+  int append;
+  int64_t n_items;
+  int num_seqs;
+  const uint16_t* k_src;
+  const uint16_t* v_src;
+  const int32_t* seq_ids;
+  const int32_t* positions;
+  const int32_t* seq_lens;
+};
+
+template <int D>
+struct QuantSmem {
+  static constexpr int kR = 0;                                    // float [D][D]
+  static constexpr int kX = kR + D * D * 4;                       // float [T][D]
+  static constexpr int kY = kX + kQTile * D * 4;                  // float [T][D]
+  static constexpr int kCodes = kY + kQTile * D * 4;              // u8 [T][D]
+  static constexpr int kSz = kCodes + kQTile * D;                 // u32 [T][ng]
+  static constexpr int kMeta = kSz + kQTile * (D / 32) * 4;       // int [6][T]
+  static constexpr int kBar = kMeta + 6 * kQTile * 4;             // u64 mbarrier
+  static constexpr int kBytes = kBar + 16;
+};
+
+__device__ __forceinline__ void flag(int32_t* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  using S = QuantSmem<D>;
+  constexpr int NG = D / 32;
+  constexpr int NW = D / 32;    // code words per lane
+  float* rs = reinterpret_cast<float*>(smem + S::kR);
+  float* xs = reinterpret_cast<float*>(smem + S::kX);
+  float* ys = reinterpret_cast<float*>(smem + S::kY);
+  uint8_t* codes = smem + S::kCodes;
+  uint32_t* szs = reinterpret_cast<uint32_t*>(smem + S::kSz);
+  int* m_i2page = reinterpret_cast<int*>(smem + S::kMeta);   // INT2 destination page (-1: none)
+  int* m_i2slot = m_i2page + kQTile;
+  int* m_bfpage = m_i2slot + kQTile;                           // BF16 destination page (-1: none)
+  int* m_bfslot = m_bfpage + kQTile;
+  int* m_srcpage = m_bfslot + kQTile;                          // append: BF16 source page
+  int* m_srcslot = m_srcpage + kQTile;
+
+  const int h = blockIdx.y;
+  const int kv = blockIdx.z;      // 0 keys, 1 values
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* rot = (kv ? p.r_v : p.r_k) + static_cast<size_t>(h) * D * D;
+  const float clip = (kv ? p.clip_v : p.clip_k)[h];
+  const uint16_t* src = kv ? p.v_src : p.k_src;
+
+  // the head's rotation arrives in shared memory by one bulk copy
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kBar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, D * D * 4);
+    bulk_g2s(rs, rot, D * D * 4, bar);
+  }
+  bool r_ready = false;
+
+  const int64_t n_tiles = (p.n_items + kQTile - 1) / kQTile;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    __syncthreads();   // previous tile's smem reads done (and R visible on the first pass)
+    int need_rot = 0;
+    if (tid < kQTile) {
+      const int64_t item = tile * kQTile + tid;
+      int i2page = -1, i2slot = 0, bfpage = -1, bfslot = 0, srcpage = -1, srcslot = 0;
+      if (item < p.n_items) {
+        if (!p.append) {
+          const int seq = p.seq_ids[item];
+          const int pos = p.positions[item];
+          const int L = (seq >= 0 && seq < p.num_seqs) ? p.seq_lens[seq] : -1;
+          if (seq < 0 || seq >= p.num_seqs || pos < 0 || pos >= L ||
+              pos / kPage >= p.max_pages) {
+            flag(p.status, OSCAR_DEVERR_SEQ_LEN);
+          } else {
+            const int64_t row = static_cast<int64_t>(seq) * p.max_pages + pos / kPage;
+            if (pos >= p.sink && pos < L - p.window) {
+              const int pg = p.int2_pt[row];
+              if (pg < 0 || pg >= p.n_int2_pages) flag(p.status, OSCAR_DEVERR_PAGE_ID);
+              else { i2page = pg; i2slot = pos % kPage; }
+            } else {
+              const int pg = p.bf16_pt[row];
+              if (pg < 0 || pg >= p.n_bf16_pages) flag(p.status, OSCAR_DEVERR_PAGE_ID);
+              else { bfpage = pg; bfslot = pos % kPage; }
+            }
+          }
+        } else {
+          const int b = static_cast<int>(item);
+          const int L = p.seq_lens[b];
+          if (L < 1 || (L - 1) / kPage >= p.max_pages) {
+            flag(p.status, OSCAR_DEVERR_SEQ_LEN);
+          } else {
+            const int64_t base = static_cast<int64_t>(b) * p.max_pages;
+            const int pn = L - 1;                      // new token -> BF16
+            const int pg = p.bf16_pt[base + pn / kPage];
+            if (pg < 0 || pg >= p.n_bf16_pages) flag(p.status, OSCAR_DEVERR_PAGE_ID);
+            else { bfpage = pg; bfslot = pn % kPage; }
+            const int po = L - 1 - p.window;           // token leaving the window
+            if (po >= p.sink) {
+              const int sp = p.bf16_pt[base + po / kPage];
+              const int dp = p.int2_pt[base + po / kPage];
+              if (sp < 0 || sp >= p.n_bf16_pages || dp < 0 || dp >= p.n_int2_pages) {
+                flag(p.status, OSCAR_DEVERR_PAGE_ID);
+              } else {
+                srcpage = sp; srcslot = po % kPage;
+                i2page = dp; i2slot = po % kPage;
+              }
+            }
+          }
+        }
+      }
+      m_i2page[tid] = i2page; m_i2slot[tid] = i2slot;
+      m_bfpage[tid] = bfpage; m_bfslot[tid] = bfslot;
+      m_srcpage[tid] = srcpage; m_srcslot[tid] = srcslot;
+      need_rot = i2page >= 0;
+    }
+    need_rot = __syncthreads_or(need_rot);
+
+    // --- load x rows (fp32) and perform the BF16 writes
+    for (int idx = tid; idx < kQTile * D; idx += kQThreads) {
+      const int t = idx / D, j = idx % D;
+      const int64_t item = tile * kQTile + t;
+      float x = 0.f;
+      if (!p.append) {
+        if (item < p.n_items) {
+          const uint16_t v = src[(item * p.hkv + h) * D + j];
+          x = bf16_to_float(v);
+          const int bp = m_bfpage[t];
+          if (bp >= 0) {
+            const int e = kv ? 16 * D + bf16_value_elem(m_bfslot[t], j) : bf16_key_elem(m_bfslot[t], j);
+            p.bf16_pool[(static_cast<int64_t>(bp) * p.hkv + h) * (32 * D) + e] = v;
+          }
+        }
+      } else if (item < p.n_items) {
+        // distinct slots: the leaving token's read and the new token's write
+        // never touch the same element
+        const int sp = m_srcpage[t];
+        if (sp >= 0) {
+          const int e = kv ? 16 * D + bf16_value_elem(m_srcslot[t], j) : bf16_key_elem(m_srcslot[t], j);
+          x = bf16_to_float(p.bf16_pool[(static_cast<int64_t>(sp) * p.hkv + h) * (32 * D) + e]);
+        }
+        const int bp = m_bfpage[t];
+        if (bp >= 0) {
+          const uint16_t v = src[(item * p.hkv + h) * D + j];
+          const int e = kv ? 16 * D + bf16_value_elem(m_bfslot[t], j) : bf16_key_elem(m_bfslot[t], j);
+          p.bf16_pool[(static_cast<int64_t>(bp) * p.hkv + h) * (32 * D) + e] = v;
+        }
+      }
+      xs[idx] = x;
+    }
+    if (!need_rot) continue;
+    if (!r_ready) {
+      r_ready = __syncthreads_and(mbar_wait(bar, 0, p.status));
+      if (!r_ready) return;   // recorded as a timeout; nothing usable to rotate with
+    }
+    __syncthreads();
+
+    // --- rotation y = x R (fp32 FMA, i ascending); warps without an INT2 token idle
+    const bool busy = m_i2page[4 * warp] >= 0 || m_i2page[4 * warp + 1] >= 0 ||
+                      m_i2page[4 * warp + 2] >= 0 || m_i2page[4 * warp + 3] >= 0;
+    if (busy) {
+      constexpr int JPT = D / 32;
+      const int jl = lane, tg = warp;
+      float acc[4][JPT];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < JPT; ++c) acc[u][c] = 0.f;
+      const float* x0 = xs + (4 * tg) * D;
+#pragma unroll 4
+      for (int i = 0; i < D; ++i) {
+        float r[JPT];
+        if constexpr (JPT == 4) {
+          const float4 v = reinterpret_cast<const float4*>(rs + i * D)[jl];
+          r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+        } else {
+          const float2 v = reinterpret_cast<const float2*>(rs + i * D)[jl];
+          r[0] = v.x; r[1] = v.y;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float xv = x0[u * D + i];
+#pragma unroll
+          for (int c = 0; c < JPT; ++c) acc[u][c] = fmaf(xv, r[c], acc[u][c]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < JPT; ++c) ys[(4 * tg + u) * D + JPT * jl + c] = acc[u][c];
+    }
+    __syncthreads();
+
+    // --- clip + group quantisation: one warp per (token, group)
+    for (int task = warp; task < kQTile * NG; task += kQThreads / 32) {
+      const int t = task / NG, grp = task % NG;
+      if (m_i2page[t] < 0) continue;
+      const float y = ys[t * D + 32 * grp + lane];
+      const float yc = fminf(fmaxf(y, -clip), clip);
+      const float mn = warp_min(yc);
+      const float mx = warp_max(yc);
+      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+      const __half z16 = __float2half_rn(mn);
+      const float sf = __half2float(s16);
+      const float zf = __half2float(z16);
+      int code = 0;
+      if (sf != 0.f) {
+        code = __float2int_rn(__fdiv_rn(__fsub_rn(yc, zf), sf));
+        code = min(max(code, 0), 3);
+      }
+      codes[t * D + 32 * grp + lane] = static_cast<uint8_t>(code);
+      if (lane == 0)
+        szs[t * NG + grp] = static_cast<uint32_t>(__half_as_ushort(s16)) |
+                            (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+    }
+    __syncthreads();
+
+    // --- pack: one thread per (token, code byte)
+    for (int idx = tid; idx < kQTile * (D / 4); idx += kQThreads) {
+      const int t = idx / (D / 4), q = idx % (D / 4);
+      const int pg = m_i2page[t];
+      if (pg < 0) continue;
+      const int slot = m_i2slot[t];
+      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(pg) * p.hkv + h) * Fmt<D>::kInt2Block;
+      const uint8_t* ct = codes + t * D;
+      uint32_t byte = 0;
+      if (kv == 0) {
+        const int tig = q / (2 * NW), m = (q >> 1) % NW, e = q & 1;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            byte |= static_cast<uint32_t>(ct[16 * (2 * m + i) + 8 * hh + 2 * tig + e]) << (4 * hh + 2 * i);
+        blk[Fmt<D>::kKc + key_byte<D>(slot, tig, m, e)] = static_cast<uint8_t>(byte);
+      } else {
+        const int gid = q / NW, m = q % NW;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            byte |= static_cast<uint32_t>(ct[16 * (2 * m + i) + 8 * ch + gid]) << (4 * ch + 2 * i);
+        blk[Fmt<D>::kVc + value_byte<D>(slot, gid, m)] = static_cast<uint8_t>(byte);
+      }
+    }
+    for (int idx = tid; idx < kQTile * NG; idx += kQThreads) {
+      const int t = idx / NG, grp = idx % NG;
+      const int pg = m_i2page[t];
+      if (pg < 0) continue;
+      const int slot = m_i2slot[t];
+      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(pg) * p.hkv + h) * Fmt<D>::kInt2Block;
+      const uint32_t sz = szs[t * NG + grp];
+      if (kv == 0) {
+        reinterpret_cast<uint32_t*>(blk + Fmt<D>::kKsz)[slot * NG + grp] = sz;
+      } else {
+        const int e = vsz_index<D>(slot, grp);
+        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
+        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVz)[e] = static_cast<uint16_t>(sz >> 16);
+      }
+    }
+  }
+  if (!r_ready) mbar_wait(bar, 0, p.status);   // never leave with the copy in flight
+}
+
+template <int D>
+oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
+  const int smem = QuantSmem<D>::kBytes;
+  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(quantize_kernel<D>), smem))
+    return OSCAR_ERR_CUDA;
+  const int64_t tiles = (p.n_items + kQTile - 1) / kQTile;
+  if (tiles == 0) return OSCAR_OK;
+  const int sms = oscar_host::sm_count();
+  const int64_t per_pair = std::max<int64_t>(1, (2LL * sms + 2 * p.hkv - 1) / (2 * p.hkv));
+  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(tiles, per_pair)), p.hkv, 2);
+  quantize_kernel<D><<<grid, kQThreads, smem, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+QuantParams base_params(const oscar_cache_desc* c) {
+  QuantParams p{};
+  p.hkv = c->num_kv_heads;
+  p.sink = c->sink;
+  p.window = c->window;
+  p.max_pages = c->max_pages_per_seq;
+  p.n_int2_pages = c->num_int2_pages;
+  p.n_bf16_pages = c->num_bf16_pages;
+  p.int2_pool = static_cast<uint8_t*>(c->int2_pool);
+  p.bf16_pool = static_cast<uint16_t*>(c->bf16_pool);
+  p.int2_pt = c->int2_page_table;
+  p.bf16_pt = c->bf16_page_table;
+  p.r_k = c->r_k;
+  p.r_v = c->r_v;
+  p.clip_k = c->clip_k;
+  p.clip_v = c->clip_v;
+  p.status = c->status;
+  return p;
+}
+
+oscar_status dispatch(const QuantParams& p, int d, cudaStream_t st) {
+  return d == 128 ? launch_quantize<128>(p, st) : launch_quantize<64>(p, st);
+}
+
+}  // namespace oscar
+
+extern "C" {
+
+oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k, const void* v,
+                                    const int32_t* seq_ids, const int32_t* positions,
+                                    const int32_t* seq_lens_final, int32_t num_seqs,
+                                    int64_t total_tokens, void* stream) {
+  oscar_status s = oscar_host::check_desc(desc, true, true);
+  if (s != OSCAR_OK) return s;
+  if (total_tokens < 0 || num_seqs < 1) return OSCAR_ERR_INVALID_ARG;
+  if (total_tokens == 0) return OSCAR_OK;
+  if (!k || !v || !seq_ids || !positions || !seq_lens_final) return OSCAR_ERR_INVALID_ARG;
+  oscar::QuantParams p = oscar::base_params(desc);
+  p.append = 0;
+  p.n_items = total_tokens;
+  p.num_seqs = num_seqs;
+  p.k_src = static_cast<const uint16_t*>(k);
+  p.v_src = static_cast<const uint16_t*>(v);
+  p.seq_ids = seq_ids;
+  p.positions = positions;
+  p.seq_lens = seq_lens_final;
+  return oscar::dispatch(p, desc->head_dim, static_cast<cudaStream_t>(stream));
+}
+
+oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_new,
+                                   const void* v_new, const int32_t* seq_lens_after,
+                                   int32_t batch, void* stream) {
+  oscar_status s = oscar_host::check_desc(desc, true, true);
+  if (s != OSCAR_OK) return s;
+  if (batch < 0) return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return OSCAR_OK;
+  if (!k_new || !v_new || !seq_lens_after) return OSCAR_ERR_INVALID_ARG;
+  oscar::QuantParams p = oscar::base_params(desc);
+  p.append = 1;
+  p.n_items = batch;
+  p.num_seqs = batch;
+  p.k_src = static_cast<const uint16_t*>(k_new);
+  p.v_src = static_cast<const uint16_t*>(v_new);
+  p.seq_lens = seq_lens_after;
+  return oscar::dispatch(p, desc->head_dim, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+"""Helpers for the GPU parity tests: upload synthetic inputs, run the library
+through its C ABI, read pools back.  Expected values come from ``oracle`` only."""
+import numpy as np
+
+from int2_rotated_kv_gb300 import pages, synth
+from oracle import attention, cache as ocache, layout
+
+DEV = "cuda:0"
+TOL_MAX_ABS = 1e-2       # attention output vs oracle (fp32 accumulate, bf16 store)
+TOL_REL_L2 = 5e-3
+
+
+def torch():
+    import torch as t
+    return t
+
+
+def lib():
+    from int2_rotated_kv_gb300 import _lib
+    _lib.lib()
+    return _lib
+
+
+def bf16_tensor(a):
+    t = torch()
+    bits = synth.bf16_bits(np.asarray(a, np.float32))
+    return t.from_numpy(bits.view(np.int16).copy()).view(t.bfloat16).to(DEV)
+
+
+def from_bf16(x):
+    t = torch()
+    return x.detach().float().cpu().numpy().astype(np.float64)
+
+
+def oracle_rotations(inst, variant=0, n_calib=None):
+    cq = inst.calib_q if n_calib is None else [x[:n_calib] for x in inst.calib_q]
+    ck = inst.calib_k if n_calib is None else [x[:n_calib] for x in inst.calib_k]
+    cv = inst.calib_v if n_calib is None else [x[:n_calib] for x in inst.calib_v]
+    return attention.calibrate(cq, ck, cv, variant)
+
+
+def make_cache(inst, rot, *, window, sink=4, growth=0, shared=0, permute=None, lens=None,
+               max_len=None):
+    w = inst.workload
+    lens = inst.seq_lens if lens is None else lens
+    pp = pages.plan(lens, sink, window, shared_prefix_tokens=shared, growth=growth,
+                    permute_seed=permute, max_len=max_len)
+    c = pages.allocate(pp, hkv=w.num_kv_heads, hq=w.num_q_heads, d=w.head_dim, sink=sink,
+                       window=window, device=DEV, r_k=np.stack(rot.rk), r_v=np.stack(rot.rv),
+                       clip_k=np.array(rot.ck, np.float32), clip_v=np.array(rot.cv, np.float32))
+    return c, pp
+
+
+def prefill(cache, inst, lens=None, upto=None):
+    """Place tokens [0, upto_b) of every sequence (default: all), final length lens."""
+    t = torch()
+    lens = inst.seq_lens if lens is None else np.asarray(lens)
+    ks, vs, sid, pos = [], [], [], []
+    for b, L in enumerate(lens):
+        n = int(L) if upto is None else int(upto[b])
+        H = inst.workload.num_kv_heads
+        ks.append(np.stack([inst.k[b][h][:n] for h in range(H)], 1))
+        vs.append(np.stack([inst.v[b][h][:n] for h in range(H)], 1))
+        sid.append(np.full(n, b, np.int32))
+        pos.append(np.arange(n, dtype=np.int32))
+    k = bf16_tensor(np.concatenate(ks))
+    v = bf16_tensor(np.concatenate(vs))
+    L = lib()
+    L.oscar_prefill_quantize(cache, k, v, t.from_numpy(np.concatenate(sid)).to(DEV),
+                             t.from_numpy(np.concatenate(pos)).to(DEV),
+                             t.from_numpy(np.asarray(lens, np.int32)).to(DEV))
+    t.cuda.synchronize()
+
+
+def pools(cache):
+    t = torch()
+    t.cuda.synchronize()
+    return cache.int2_pool.cpu().numpy(), cache.bf16_pool.view(t.int16).cpu().numpy().view(np.uint16)
+
+
+def expected(inst, rot, pp, *, window, sink=4, lens=None, kappa=None):
+    w = inst.workload
+    lens = inst.seq_lens if lens is None else lens
+    return ocache.expected_pools(inst.k, inst.v, lens, rot, sink=sink, window=window,
+                                 d=w.head_dim, hkv=w.num_kv_heads, int2_table=pp.int2_table,
+                                 bf16_table=pp.bf16_table, num_int2_pages=pp.num_int2_pages,
+                                 num_bf16_pages=pp.num_bf16_pages, kappa=kappa)
+
+
+def compare_pools(cache, exp):
+    """Bit-exact on every byte the oracle defines, except bytes of flagged
+    near-boundary entries; returns (#mismatched flagged bytes, #flagged bytes)."""
+    got2, gotb = pools(cache)
+    bad = exp.int2_defined & ~exp.int2_maydiffer & (got2 != exp.int2)
+    assert not bad.any(), f"{int(bad.sum())} INT2 bytes differ outside flagged entries; first at {np.flatnonzero(bad)[:8]}"
+    badb = exp.bf16_defined & (gotb != exp.bf16)
+    assert not badb.any(), f"{int(badb.sum())} BF16 elements differ"
+    flagged = exp.int2_defined & exp.int2_maydiffer
+    return int((flagged & (got2 != exp.int2)).sum()), int(flagged.sum())
+
+
+def decode(cache, q, lens, max_len=None, bf16_only=False, out=None):
+    t = torch()
+    L = lib()
+    lens = np.asarray(lens, np.int32)
+    max_len = int(lens.max()) if max_len is None else max_len
+    B, Hq, d = q.shape
+    qt = bf16_tensor(q)
+    o = t.zeros((B, Hq, d), dtype=t.bfloat16, device=DEV) if out is None else out
+    ws_bytes = L.oscar_decode_workspace_size(cache, B, max_len)
+    ws = t.empty(ws_bytes // 4 + 64, dtype=t.float32, device=DEV)
+    lt = t.from_numpy(lens).to(DEV)
+    fn = L.oscar_decode_attention_bf16 if bf16_only else L.oscar_decode_attention
+    fn(cache, qt, lt, max_len, o, ws)
+    t.cuda.synchronize()
+    return from_bf16(o)
+
+
+def status(cache):
+    return int(cache.status.cpu().item())
+
+
+def bf16_half_ulp(x):
+    """Half a bf16 ulp at |x| (8 significant bits): the store's own rounding."""
+    x = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(x)) - 8)
+
+
+def check_close(got, ref, what=""):
+    """Output parity: rel-L2 <= 5e-3 and, per element, |got - ref| <= 1e-2 plus
+    half a bf16 ulp of ref (the output is stored in bf16; for |out| >= 4 the
+    rounding of an exact result alone can exceed 1e-2)."""
+    dev = np.abs(got - ref)
+    excess = dev - bf16_half_ulp(ref)
+    err = float(dev.max())
+    worst = float(excess.max())
+    rel = attention.rel_l2(got, ref)
+    assert worst <= TOL_MAX_ABS and rel <= TOL_REL_L2, \
+        f"{what}: max-abs {err:.3e} (beyond bf16 rounding {worst:.3e}), rel-L2 {rel:.3e}"
+    return err, rel
+
+
+def kappa(d):
+    # sequential fp32 FMA chain of d terms: |error| <= d * 2^-24 * sum |x_i R_ij|
+    return 1.01 * d * 2.0 ** -24
