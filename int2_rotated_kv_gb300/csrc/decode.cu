@@ -66,27 +66,32 @@ struct DecodeParams {
   float* qrot;    // [B][Hq][D]
   float* part;    // [B][Hq][n_splits][D + 2]
   float scale_log2;
+  int wait_first; // wait for the predecessor grid before reading any input
 };
 
 // ------------------------------------------------------------------ q R_K
 
 template <int D>
 __global__ void __launch_bounds__(1024) qrot_kernel(const DecodeParams p) {
+  // the caller's earlier work (q, rotations, cache writes) is complete after the
+  // wait; only then may the split kernel launch and prefetch pages
+  pdl_wait();
   pdl_trigger();
   __shared__ float qs[8][D];
   __shared__ float partial[1024 / D][8][D];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int G = p.G;
-  for (int i = tid; i < G * D; i += blockDim.x)
-    qs[i / D][i % D] = bf16_to_float(p.q[(static_cast<size_t>(b) * p.hq + h * G) * D + i]);
-  __syncthreads();
   constexpr int CH = 1024 / D;          // chunks of the contraction index
   constexpr int PER = D / CH;
   const int j = tid % D, c = tid / D;
+  // the rotation and the query are fetched in the same round trip
   const float* r = p.r_k + static_cast<size_t>(h) * D * D;
   float rv[PER];
 #pragma unroll
   for (int u = 0; u < PER; ++u) rv[u] = r[(c * PER + u) * D + j];
+  for (int i = tid; i < G * D; i += blockDim.x)
+    qs[i / D][i % D] = bf16_to_float(p.q[(static_cast<size_t>(b) * p.hq + h * G) * D + i]);
+  __syncthreads();
   for (int g = 0; g < G; ++g) {
     float acc = 0.f;
 #pragma unroll
@@ -120,6 +125,7 @@ struct SplitCfg {
   static constexpr int kRingOff = kBars + kDWarps * 8 * 8;
   static constexpr int kBytes = kRingOff + kRing;
   static constexpr int kCtasPerSm = kBf16Only ? 1 : 2;
+  static_assert(kStagesI <= 8 && kStagesB <= 8, "eight mbarriers per warp");
 };
 
 struct Softmax {
@@ -128,21 +134,24 @@ struct Softmax {
 
 // Online-softmax update for one 16-token tile.  l[] are log2-domain logits in
 // the m16n8 accumulator layout (rows = tokens gid / gid+8, cols = query heads
-// 2tig / 2tig+1).  Rescales the output accumulators when the max grows and
-// returns the probabilities in p[].
+// 2tig / 2tig+1).  The running max is only raised (cross-lane reduction plus
+// rescale of the accumulators) when some logit exceeds it by more than kTau,
+// so most tiles skip the shuffles; probabilities stay <= 2^kTau.
+constexpr float kTau = 8.f;
+
 template <int NT>
 __device__ __forceinline__ void softmax_tile(Softmax& st, float (&l)[4], float (&o)[NT][4],
                                              float (&z)[4], float (&pr)[4]) {
   float mx0 = fmaxf(l[0], l[2]), mx1 = fmaxf(l[1], l[3]);
+  if (__any_sync(0xffffffffu, mx0 > st.m0 + kTau || mx1 > st.m1 + kTau)) {
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-  }
-  const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
-  if (n0 > st.m0 || n1 > st.m1) {
-    const float a0 = (n0 == st.m0) ? 1.f : exp2f(st.m0 - n0);
-    const float a1 = (n1 == st.m1) ? 1.f : exp2f(st.m1 - n1);
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
+    const float a0 = (n0 == st.m0) ? 1.f : fast_exp2(st.m0 - n0);
+    const float a1 = (n1 == st.m1) ? 1.f : fast_exp2(st.m1 - n1);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       o[t][0] *= a0; o[t][2] *= a0;
@@ -154,10 +163,10 @@ __device__ __forceinline__ void softmax_tile(Softmax& st, float (&l)[4], float (
   }
   const float b0 = st.m0 == -INFINITY ? 0.f : st.m0;
   const float b1 = st.m1 == -INFINITY ? 0.f : st.m1;
-  pr[0] = exp2f(l[0] - b0);
-  pr[1] = exp2f(l[1] - b1);
-  pr[2] = exp2f(l[2] - b0);
-  pr[3] = exp2f(l[3] - b1);
+  pr[0] = fast_exp2(l[0] - b0);
+  pr[1] = fast_exp2(l[1] - b1);
+  pr[2] = fast_exp2(l[2] - b0);
+  pr[3] = fast_exp2(l[3] - b1);
   st.l0 += pr[0] + pr[2];
   st.l1 += pr[1] + pr[3];
 }
@@ -167,6 +176,287 @@ __device__ __forceinline__ bool tok_ok(int t, int L, int sink, int window, int m
   if (mode == 0) return t >= sink && t < L - window;
   if (mode == 1) return t < L && (t < sink || t >= L - window);
   return t < L;
+}
+
+// Bounded wait on one stage; a timeout drains the copies still in flight (with
+// the same bound) and reports false so the caller stops.
+template <int NS>
+__device__ __forceinline__ bool wait_stage(uint64_t* wbar, int s, uint32_t& phase, int i, int my_n,
+                                           const int* ids, int warp, int32_t* status) {
+  const bool ok = mbar_wait(&wbar[s], (phase >> s) & 1u, status);
+  phase ^= 1u << s;
+  if (__all_sync(0xffffffffu, ok)) return true;
+  for (int j = i + 1; j < min(i + NS, my_n); ++j) {
+    if (ids[warp + kDWarps * j] >= 0) {
+      const int sj = j % NS;
+      mbar_wait(&wbar[sj], (phase >> sj) & 1u, status);
+      phase ^= 1u << sj;
+    }
+  }
+  return false;
+}
+
+// INT2 pages [lo, lo + n) of one (sequence, KV head): warp w takes pages
+// w, w + 8, ... through its own ring of NS bulk-copied page-head blocks.
+template <int D, int NS>
+__device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, int warp, int lane,
+                                           const int* ids, int lo, int n, int L, uint8_t* ring,
+                                           uint64_t* bars, float (&o)[D / 16][4], float (&zacc)[4],
+                                           Softmax& sm) {
+  constexpr int NG = D / 32, NK = D / 16;
+  constexpr int SB = Fmt<D>::kInt2Block;
+  const int gid = lane >> 2, tig = lane & 3, G = p.G;
+  uint8_t* wring = ring + warp * NS * SB;
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(bars) + warp * 8;
+  const uint8_t* pool_h = p.int2_pool + static_cast<size_t>(h) * SB;
+  const size_t pstride = static_cast<size_t>(p.hkv) * SB;
+  const int my_n = n > warp ? (n - warp + kDWarps - 1) / kDWarps : 0;
+  if (lane == 0) {
+    for (int i = 0; i < min(NS, my_n); ++i) {
+      const int id = ids[warp + kDWarps * i];
+      if (id >= 0) {
+        mbar_arrive_expect_tx(&wbar[i], SB);
+        bulk_g2s(wring + i * SB, pool_h + id * pstride, SB, &wbar[i]);
+      }
+    }
+  }
+  // ---- query operand, once the rotated query is complete
+  pdl_wait();
+  uint32_t qb[NK][2];
+  uint32_t qz = 0;
+  {
+    const float* qr = p.qrot + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
+    float gs[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) gs[g] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+      float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
+      if (gid < G) {
+        v0 = *reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig);
+        v1 = *reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig + 8);
+      }
+      gs[kk >> 1] += (v0.x + v0.y) + (v1.x + v1.y);
+      // codes of k-step parity i and channel half h are read at 4^i * 16^h
+      const float sc = (kk & 1) ? 0.25f : 1.f;
+      qb[kk][0] = pack_half2(v0.x * sc, v0.y * sc);
+      qb[kk][1] = pack_half2(v1.x * sc * 0.0625f, v1.y * sc * 0.0625f);
+    }
+    float mine = 0.f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      gs[g] += __shfl_xor_sync(0xffffffffu, gs[g], 1);
+      gs[g] += __shfl_xor_sync(0xffffffffu, gs[g], 2);
+      if (g == tig) mine = gs[g];
+    }
+    if (tig < NG) {   // zero-term operand, pre-scaled to log2-domain logits
+      mine *= p.scale_log2;
+      const __half hi = __float2half_rn(mine);
+      const __half lo16 = __float2half_rn(mine - __half2float(hi));
+      qz = static_cast<uint32_t>(__half_as_ushort(hi)) |
+           (static_cast<uint32_t>(__half_as_ushort(lo16)) << 16);
+    }
+  }
+  const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
+  const int tok_lo = p.sink, tok_hi = L - p.window;
+  uint32_t phase = 0;
+  int s = 0;
+  for (int i = 0; i < my_n; ++i) {
+    const int k = warp + kDWarps * i;
+    if (ids[k] >= 0) {
+      if (!wait_stage<NS>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
+      const uint8_t* st = wring + s * SB;
+      // ---- q.K over exact 2-bit codes, one accumulator per group
+      uint32_t kw[NG];
+      if constexpr (NG == 4) {
+        const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kKc)[lane];
+        kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
+      } else {
+        const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kKc)[lane];
+        kw[0] = v.x; kw[1] = v.y;
+      }
+      float dg[NG][4];
+#pragma unroll
+      for (int m = 0; m < NG; ++m) {
+        // pair (s, i) sits at bits 4s+2i (+16); s = 2, 3 are reached with one
+        // shift by 8, so every extracted half is code * 4^i * 16^(s&1) * 2^-24
+        const uint32_t wl = kw[m], wh = kw[m] >> 8;
+        const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
+        // A registers a0..a3 hold key pairs s = 0, 2, 1, 3
+        mma_f16_z(dg[m], wl & m0, wh & m0, wl & m1, wh & m1, qb[2 * m][0], qb[2 * m][1]);
+        mma_f16(dg[m], wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2),
+                qb[2 * m + 1][0], qb[2 * m + 1][1]);
+      }
+      const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kKsz);
+      uint32_t za = 0, zb = 0;
+      if (tig < NG) {
+        const uint32_t e0 = ksz[gid * NG + tig], e1 = ksz[(gid + 8) * NG + tig];
+        za = __byte_perm(e0, e0, 0x3232);
+        zb = __byte_perm(e1, e1, 0x3232);
+      }
+      float lg[4];
+      mma_f16_z(lg, za, zb, 0u, 0u, qz, 0u);       // zero term, already in log2 units
+      uint32_t sa[NG], sb[NG];
+      if constexpr (NG == 4) {
+        const uint4 a = reinterpret_cast<const uint4*>(ksz)[gid];
+        const uint4 c = reinterpret_cast<const uint4*>(ksz)[gid + 8];
+        sa[0] = a.x; sa[1] = a.y; sa[2] = a.z; sa[3] = a.w;
+        sb[0] = c.x; sb[1] = c.y; sb[2] = c.z; sb[3] = c.w;
+      } else {
+        const uint2 a = reinterpret_cast<const uint2*>(ksz)[gid];
+        const uint2 c = reinterpret_cast<const uint2*>(ksz)[gid + 8];
+        sa[0] = a.x; sa[1] = a.y;
+        sb[0] = c.x; sb[1] = c.y;
+      }
+#pragma unroll
+      for (int m = 0; m < NG; ++m) {
+        const float fa = half_lo(sa[m]) * ks, fb = half_lo(sb[m]) * ks;
+        lg[0] = fmaf(fa, dg[m][0], lg[0]);
+        lg[1] = fmaf(fa, dg[m][1], lg[1]);
+        lg[2] = fmaf(fb, dg[m][2], lg[2]);
+        lg[3] = fmaf(fb, dg[m][3], lg[3]);
+      }
+      // tokens outside [sink, L - window) only occur on the range's end pages
+      const int pbeg = (lo + k) * kPage;
+      if (pbeg < tok_lo || pbeg + kPage > tok_hi) {
+        const int t0 = pbeg + gid, t1 = t0 + 8;
+        if (t0 < tok_lo || t0 >= tok_hi) lg[0] = lg[1] = -INFINITY;
+        if (t1 < tok_lo || t1 >= tok_hi) lg[2] = lg[3] = -INFINITY;
+      }
+      float pr[4];
+      softmax_tile<NK>(sm, lg, o, zacc, pr);
+      // ---- p.V over exact 2-bit codes, p * s per group as the B operand
+      const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0], pr[1]));
+      const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2], pr[3]));
+      uint32_t vw[NG], vs0[NG], vs1[NG];
+      const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVs);
+      if constexpr (NG == 4) {
+        const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kVc)[lane];
+        vw[0] = v.x; vw[1] = v.y; vw[2] = v.z; vw[3] = v.w;
+        const uint4 a = reinterpret_cast<const uint4*>(vsw)[tig * 2];
+        const uint4 c = reinterpret_cast<const uint4*>(vsw)[tig * 2 + 1];
+        vs0[0] = a.x; vs0[1] = a.y; vs0[2] = a.z; vs0[3] = a.w;
+        vs1[0] = c.x; vs1[1] = c.y; vs1[2] = c.z; vs1[3] = c.w;
+      } else {
+        const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kVc)[lane];
+        vw[0] = v.x; vw[1] = v.y;
+        const uint2 a = reinterpret_cast<const uint2*>(vsw)[tig * 2];
+        const uint2 c = reinterpret_cast<const uint2*>(vsw)[tig * 2 + 1];
+        vs0[0] = a.x; vs0[1] = a.y;
+        vs1[0] = c.x; vs1[1] = c.y;
+      }
+#pragma unroll
+      for (int m = 0; m < NG; ++m) {
+        const uint32_t bb0 = hmul2_u32(pb0, vs0[m]);
+        const uint32_t bb1 = hmul2_u32(pb1, vs1[m]);
+        // value pair s = r: rows gid (s = 0, 2) read at 4^i, rows gid+8 (s = 1, 3) at 16 * 4^i
+        const uint32_t wl = vw[m], wh = vw[m] >> 8;
+        const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
+        mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bb0, bb1);
+        mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
+                bb0, bb1);
+      }
+      const uint32_t* vz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVz);
+      uint32_t za0 = 0, za2 = 0;
+      if (gid < NG) {
+        za0 = vz[(tig * 2) * NG + gid];
+        za2 = vz[(tig * 2 + 1) * NG + gid];
+      }
+      mma_f16(zacc, za0, 0u, za2, 0u, pb0, pb1);
+    }
+    // refill this stage once every lane is done reading it (the warp barrier
+    // orders the reads before the bulk copy that overwrites the stage)
+    __syncwarp();
+    if (lane == 0 && i + NS < my_n) {
+      const int id = ids[k + kDWarps * NS];
+      if (id >= 0) {
+        mbar_arrive_expect_tx(&wbar[s], SB);
+        bulk_g2s(wring + s * SB, pool_h + id * pstride, SB, &wbar[s]);
+      }
+    }
+    s = (s + 1 == NS) ? 0 : s + 1;
+  }
+}
+
+// BF16 pages (the sink + recent split, or every page of the BF16 baseline):
+// raw q against bf16 keys and values in the same fragment-native order.
+template <int D, int NS>
+__device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, int warp, int lane,
+                                           const int* ids, const int* lps, int n, int L, int mode,
+                                           uint8_t* ring, uint64_t* bars, float (&o)[D / 16][4],
+                                           Softmax& sm) {
+  constexpr int NK = D / 16;
+  constexpr int SB = Fmt<D>::kBf16Block;
+  const int gid = lane >> 2, tig = lane & 3, G = p.G;
+  uint8_t* wring = ring + warp * NS * SB;
+  uint64_t* wbar = bars + warp * 8;
+  const uint8_t* pool_h = p.bf16_pool + static_cast<size_t>(h) * SB;
+  const size_t pstride = static_cast<size_t>(p.hkv) * SB;
+  const int my_n = n > warp ? (n - warp + kDWarps - 1) / kDWarps : 0;
+  if (lane == 0) {
+    for (int i = 0; i < min(NS, my_n); ++i) {
+      const int id = ids[warp + kDWarps * i];
+      if (id >= 0) {
+        mbar_arrive_expect_tx(&wbar[i], SB);
+        bulk_g2s(wring + i * SB, pool_h + id * pstride, SB, &wbar[i]);
+      }
+    }
+  }
+  pdl_wait();
+  uint32_t qb[NK][2];
+  {
+    const uint16_t* qr = p.q + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+      qb[kk][0] = gid < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig) : 0u;
+      qb[kk][1] = gid < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig + 8) : 0u;
+    }
+  }
+  const float scale_log2 = p.scale_log2;
+  float zdummy[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t phase = 0;
+  int s = 0;
+  for (int i = 0; i < my_n; ++i) {
+    const int k = warp + kDWarps * i;
+    if (ids[k] >= 0) {
+      if (!wait_stage<NS>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
+      const uint8_t* st = wring + s * SB;
+      float dk[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4* kb = reinterpret_cast<const uint4*>(st);
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        const uint4 a = kb[kk * 32 + lane];
+        mma_bf16(dk, a.x, a.y, a.z, a.w, qb[kk][0], qb[kk][1]);
+      }
+      float lg[4] = {dk[0] * scale_log2, dk[1] * scale_log2, dk[2] * scale_log2, dk[3] * scale_log2};
+      const int pbeg = lps[k] * kPage;
+      const bool whole = mode == 2 && pbeg + kPage <= L;
+      if (!whole) {
+        const int t0 = pbeg + gid, t1 = t0 + 8;
+        if (!tok_ok(t0, L, p.sink, p.window, mode)) lg[0] = lg[1] = -INFINITY;
+        if (!tok_ok(t1, L, p.sink, p.window, mode)) lg[2] = lg[3] = -INFINITY;
+      }
+      float pr[4];
+      softmax_tile<NK>(sm, lg, o, zdummy, pr);
+      const uint32_t pb0 = movmatrix_trans(pack_bf162(pr[0], pr[1]));
+      const uint32_t pb1 = movmatrix_trans(pack_bf162(pr[2], pr[3]));
+      const uint4* vb = reinterpret_cast<const uint4*>(st + Fmt<D>::kBf16V);
+#pragma unroll
+      for (int mt = 0; mt < NK; ++mt) {
+        const uint4 a = vb[mt * 32 + lane];
+        mma_bf16(o[mt], a.x, a.y, a.z, a.w, pb0, pb1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + NS < my_n) {
+      const int id = ids[k + kDWarps * NS];
+      if (id >= 0) {
+        mbar_arrive_expect_tx(&wbar[s], SB);
+        bulk_g2s(wring + s * SB, pool_h + id * pstride, SB, &wbar[s]);
+      }
+    }
+    s = (s + 1 == NS) ? 0 : s + 1;
+  }
 }
 
 template <int D, bool kBf16Only>
@@ -186,14 +476,30 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   const int gid = lane >> 2, tig = lane & 3;
   const int G = p.G;
 
+  // Without a gate kernel in front (the BF16-only call), nothing may be read
+  // before the predecessor grid completes.
+  if (p.wait_first) pdl_wait();
+  // main splits know their page span without the length, so the page ids are
+  // fetched in the same round trip as the length
+  const bool bf16_split = kBf16Only || split == p.n_main;
+  const int mode = kBf16Only ? 2 : (bf16_split ? 1 : 0);
+  const int first = mode == 0 ? p.sink / kPage : 0;
+  const int lo = first + split * p.pps;
+  const int32_t* pt = (mode == 0 ? p.int2_pt : p.bf16_pt) + static_cast<size_t>(b) * p.max_pages;
+  const int64_t npages = mode == 0 ? p.n_int2_pages : p.n_bf16_pages;
+  int spec[(kMaxCtaPages + kDThreads - 1) / kDThreads];
+  if (mode != 1) {
+#pragma unroll
+    for (int r = 0; r < (kMaxCtaPages + kDThreads - 1) / kDThreads; ++r) {
+      const int k = tid + r * kDThreads;
+      spec[r] = (k < p.pps && lo + k < p.max_pages) ? pt[lo + k] : -1;
+    }
+  }
   int L = p.seq_lens[b];
   if (L < 1 || L > p.max_len) {
     if (tid == 0 && p.status) atomicOr(p.status, OSCAR_DEVERR_SEQ_LEN);
     L = 0;
   }
-  // ---- which pages this CTA reads
-  const bool bf16_split = kBf16Only || split == p.n_main;
-  const int mode = kBf16Only ? 2 : (bf16_split ? 1 : 0);
   int n = 0;
   if (mode == 1) {
     // sink pages, then recent pages not already listed
@@ -203,27 +509,9 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
     const int r0 = max(r_beg, s_end);
     const int n_sink = s_end, n_rec = max(0, r_end - r0);
     n = min(n_sink + n_rec, kMaxCtaPages);
-    for (int k = tid; k < n; k += kDThreads) lps[k] = k < n_sink ? k : r0 + (k - n_sink);
-  } else {
-    int first, last;   // logical page span of the main region
-    if (mode == 0) {
-      first = p.sink / kPage;
-      last = (L - p.window > p.sink) ? (L - p.window + kPage - 1) / kPage : first;
-    } else {
-      first = 0;
-      last = (L + kPage - 1) / kPage;
-    }
-    const int lo = first + split * p.pps;
-    const int hi = min(last, lo + p.pps);
-    n = max(0, min(hi - lo, kMaxCtaPages));
-    for (int k = tid; k < n; k += kDThreads) lps[k] = lo + k;
-  }
-  __syncthreads();
-  {
-    const int32_t* pt = (mode == 0 ? p.int2_pt : p.bf16_pt) + static_cast<size_t>(b) * p.max_pages;
-    const int64_t npages = mode == 0 ? p.n_int2_pages : p.n_bf16_pages;
     for (int k = tid; k < n; k += kDThreads) {
-      const int lp = lps[k];
+      const int lp = k < n_sink ? k : r0 + (k - n_sink);
+      lps[k] = lp;
       int id = lp < p.max_pages ? pt[lp] : -1;
       if (id < 0 || id >= npages) {
         if (p.status) atomicOr(p.status, OSCAR_DEVERR_PAGE_ID);
@@ -231,231 +519,38 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
       }
       ids[k] = id;
     }
+  } else {
+    const int last = mode == 0
+        ? ((L - p.window > p.sink) ? (L - p.window + kPage - 1) / kPage : first)
+        : (L + kPage - 1) / kPage;
+    n = max(0, min(min(last, lo + p.pps) - lo, kMaxCtaPages));
+#pragma unroll
+    for (int r = 0; r < (kMaxCtaPages + kDThreads - 1) / kDThreads; ++r) {
+      const int k = tid + r * kDThreads;
+      if (k < n) {
+        int id = spec[r];
+        if (id < 0 || id >= npages) {
+          if (p.status) atomicOr(p.status, OSCAR_DEVERR_PAGE_ID);
+          id = -1;
+        }
+        ids[k] = id;
+        lps[k] = lo + k;
+      }
+    }
   }
   if (tid < kDWarps * 8) mbar_init(&bars[tid], 1);
   fence_mbar_init();
   __syncthreads();
-
-  // ---- per-warp ring
-  const int stage_bytes = mode == 0 ? Fmt<D>::kInt2Block : Fmt<D>::kBf16Block;
-  const int n_stages = mode == 0 ? C::kStagesI : C::kStagesB;
-  uint8_t* wring = ring + warp * n_stages * stage_bytes;
-  uint64_t* wbar = bars + warp * 8;
-  const uint8_t* pool = mode == 0 ? p.int2_pool : p.bf16_pool;
-  const int my_n = n > warp ? (n - warp + kDWarps - 1) / kDWarps : 0;
-
-  auto issue = [&](int i) {
-    const int id = ids[warp + kDWarps * i];
-    if (id < 0) return;
-    const int s = i % n_stages;
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&wbar[s], stage_bytes);
-    bulk_g2s(wring + s * stage_bytes,
-             pool + (static_cast<size_t>(id) * p.hkv + h) * stage_bytes, stage_bytes, &wbar[s]);
-  };
-  if (lane == 0)
-    for (int i = 0; i < min(n_stages, my_n); ++i) issue(i);
-
-  // ---- query operand (B fragments), after the producer of q' has finished
-  pdl_wait();
-  uint32_t qb[NK][2];
-  uint32_t qz = 0;
-  const float scale_log2 = p.scale_log2;
-  if (mode == 0) {
-    const float* qr = p.qrot + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
-    float gs[NG];
-#pragma unroll
-    for (int g = 0; g < NG; ++g) gs[g] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < NK; ++kk) {
-      float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
-      if (gid < G) {
-        v0 = *reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig);
-        v1 = *reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig + 8);
-      }
-      gs[kk >> 1] += (v0.x + v0.y) + (v1.x + v1.y);
-      const float sc = (kk & 1) ? 0.25f : 1.f;   // odd k-steps read codes at 4x
-      qb[kk][0] = pack_half2(v0.x * sc, v0.y * sc);
-      qb[kk][1] = pack_half2(v1.x * sc, v1.y * sc);
-    }
-    float mine = 0.f;
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      gs[g] += __shfl_xor_sync(0xffffffffu, gs[g], 1);
-      gs[g] += __shfl_xor_sync(0xffffffffu, gs[g], 2);
-      if (g == tig) mine = gs[g];
-    }
-    if (tig < NG) {
-      const __half hi = __float2half_rn(mine);
-      const __half lo = __float2half_rn(mine - __half2float(hi));
-      qz = static_cast<uint32_t>(__half_as_ushort(hi)) |
-           (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
-    }
-  } else {
-    const uint16_t* qr = p.q + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
-#pragma unroll
-    for (int kk = 0; kk < NK; ++kk) {
-      qb[kk][0] = gid < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig) : 0u;
-      qb[kk][1] = gid < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig + 8) : 0u;
-    }
-  }
 
   float o[NK][4];
 #pragma unroll
   for (int t = 0; t < NK; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
   float zacc[4] = {0.f, 0.f, 0.f, 0.f};
   Softmax sm{-INFINITY, -INFINITY, 0.f, 0.f};
-  uint32_t phase = 0;
-  const float ks = scale_log2 * 16777216.f;   // codes are read as code * 2^-24
-
-  for (int i = 0; i < my_n; ++i) {
-    const int k = warp + kDWarps * i;
-    const int s = i % n_stages;
-    if (ids[k] >= 0) {
-      const bool ok = mbar_wait(&wbar[s], (phase >> s) & 1u, p.status);
-      phase ^= 1u << s;
-      if (__any_sync(0xffffffffu, !ok)) {
-        // give the copies still in flight a bounded chance to land, then stop
-        for (int j = i + 1; j < min(i + n_stages, my_n); ++j)
-          if (ids[warp + kDWarps * j] >= 0) {
-            const int sj = j % n_stages;
-            mbar_wait(&wbar[sj], (phase >> sj) & 1u, p.status);
-            phase ^= 1u << sj;
-          }
-        break;
-      }
-      const uint8_t* st = wring + s * stage_bytes;
-      const int t0 = lps[k] * kPage + gid, t1 = t0 + 8;
-      float lg[4], pr[4];
-      if (mode == 0) {
-        // ---- q.K over exact 2-bit codes, per-group accumulators
-        uint32_t kw[NG];
-        if constexpr (NG == 4) {
-          const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kKc)[lane];
-          kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
-        } else {
-          const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kKc)[lane];
-          kw[0] = v.x; kw[1] = v.y;
-        }
-        float dg[NG][4];
-#pragma unroll
-        for (int m = 0; m < NG; ++m) {
-          dg[m][0] = dg[m][1] = dg[m][2] = dg[m][3] = 0.f;
-          const uint32_t w0 = kw[m], w1 = w0 >> 4, w2 = w0 >> 8, w3 = w0 >> 12;
-#pragma unroll
-          for (int ii = 0; ii < 2; ++ii) {
-            const uint32_t mask = 0x00030003u << (2 * ii);
-            // A registers a0..a3 hold (s = 0, 2, 1, 3) for keys
-            mma_f16(dg[m], w0 & mask, w2 & mask, w1 & mask, w3 & mask, qb[2 * m + ii][0],
-                    qb[2 * m + ii][1]);
-          }
-        }
-        const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kKsz);
-        uint32_t za = 0, zb = 0;
-        if (tig < NG) {
-          const uint32_t e0 = ksz[gid * NG + tig], e1 = ksz[(gid + 8) * NG + tig];
-          za = __byte_perm(e0, e0, 0x3232);
-          zb = __byte_perm(e1, e1, 0x3232);
-        }
-        float zq[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16(zq, za, zb, 0u, 0u, qz, 0u);
-        uint32_t sa[NG], sb[NG];
-        if constexpr (NG == 4) {
-          const uint4 a = reinterpret_cast<const uint4*>(ksz)[gid];
-          const uint4 c = reinterpret_cast<const uint4*>(ksz)[gid + 8];
-          sa[0] = a.x; sa[1] = a.y; sa[2] = a.z; sa[3] = a.w;
-          sb[0] = c.x; sb[1] = c.y; sb[2] = c.z; sb[3] = c.w;
-        } else {
-          const uint2 a = reinterpret_cast<const uint2*>(ksz)[gid];
-          const uint2 c = reinterpret_cast<const uint2*>(ksz)[gid + 8];
-          sa[0] = a.x; sa[1] = a.y;
-          sb[0] = c.x; sb[1] = c.y;
-        }
-        lg[0] = zq[0] * scale_log2; lg[1] = zq[1] * scale_log2;
-        lg[2] = zq[2] * scale_log2; lg[3] = zq[3] * scale_log2;
-#pragma unroll
-        for (int m = 0; m < NG; ++m) {
-          const float fa = half_lo(sa[m]) * ks, fb = half_lo(sb[m]) * ks;
-          lg[0] = fmaf(fa, dg[m][0], lg[0]);
-          lg[1] = fmaf(fa, dg[m][1], lg[1]);
-          lg[2] = fmaf(fb, dg[m][2], lg[2]);
-          lg[3] = fmaf(fb, dg[m][3], lg[3]);
-        }
-      } else {
-        // ---- q.K over bf16 keys
-        float dk[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint4* kb = reinterpret_cast<const uint4*>(st);
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-          const uint4 a = kb[kk * 32 + lane];
-          mma_bf16(dk, a.x, a.y, a.z, a.w, qb[kk][0], qb[kk][1]);
-        }
-        lg[0] = dk[0] * scale_log2; lg[1] = dk[1] * scale_log2;
-        lg[2] = dk[2] * scale_log2; lg[3] = dk[3] * scale_log2;
-      }
-      // mask tokens outside this CTA's region (only on boundary pages)
-      const int pbeg = lps[k] * kPage;
-      const bool whole = mode == 2 ? (pbeg + kPage <= L)
-                       : mode == 0 ? (pbeg >= p.sink && pbeg + kPage <= L - p.window)
-                                   : false;
-      if (!whole) {
-        if (!tok_ok(t0, L, p.sink, p.window, mode)) lg[0] = lg[1] = -INFINITY;
-        if (!tok_ok(t1, L, p.sink, p.window, mode)) lg[2] = lg[3] = -INFINITY;
-      }
-      softmax_tile<NK>(sm, lg, o, zacc, pr);
-
-      if (mode == 0) {
-        const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0], pr[1]));
-        const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2], pr[3]));
-        uint32_t vw[NG], vs0[NG], vs1[NG];
-        const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVs);
-        if constexpr (NG == 4) {
-          const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kVc)[lane];
-          vw[0] = v.x; vw[1] = v.y; vw[2] = v.z; vw[3] = v.w;
-          const uint4 a = reinterpret_cast<const uint4*>(vsw)[tig * 2];
-          const uint4 c = reinterpret_cast<const uint4*>(vsw)[tig * 2 + 1];
-          vs0[0] = a.x; vs0[1] = a.y; vs0[2] = a.z; vs0[3] = a.w;
-          vs1[0] = c.x; vs1[1] = c.y; vs1[2] = c.z; vs1[3] = c.w;
-        } else {
-          const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kVc)[lane];
-          vw[0] = v.x; vw[1] = v.y;
-          const uint2 a = reinterpret_cast<const uint2*>(vsw)[tig * 2];
-          const uint2 c = reinterpret_cast<const uint2*>(vsw)[tig * 2 + 1];
-          vs0[0] = a.x; vs0[1] = a.y;
-          vs1[0] = c.x; vs1[1] = c.y;
-        }
-#pragma unroll
-        for (int m = 0; m < NG; ++m) {
-          const uint32_t bb0 = hmul2_u32(pb0, vs0[m]);
-          const uint32_t bb1 = hmul2_u32(pb1, vs1[m]);
-          const uint32_t w0 = vw[m], w1 = w0 >> 4, w2 = w0 >> 8, w3 = w0 >> 12;
-#pragma unroll
-          for (int ii = 0; ii < 2; ++ii) {
-            const uint32_t mask = 0x00030003u << (2 * ii);
-            mma_f16(o[2 * m + ii], w0 & mask, w1 & mask, w2 & mask, w3 & mask, bb0, bb1);
-          }
-        }
-        const uint32_t* vz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVz);
-        uint32_t za0 = 0, za2 = 0;
-        if (gid < NG) {
-          za0 = vz[(tig * 2) * NG + gid];
-          za2 = vz[(tig * 2 + 1) * NG + gid];
-        }
-        mma_f16(zacc, za0, 0u, za2, 0u, pb0, pb1);
-      } else {
-        const uint32_t pb0 = movmatrix_trans(pack_bf162(pr[0], pr[1]));
-        const uint32_t pb1 = movmatrix_trans(pack_bf162(pr[2], pr[3]));
-        const uint4* vb = reinterpret_cast<const uint4*>(st + Fmt<D>::kBf16V);
-#pragma unroll
-        for (int mt = 0; mt < NK; ++mt) {
-          const uint4 a = vb[mt * 32 + lane];
-          mma_bf16(o[mt], a.x, a.y, a.z, a.w, pb0, pb1);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0 && i + n_stages < my_n) issue(i + n_stages);
-  }
+  if (mode == 0)
+    int2_pages<D, C::kStagesI>(p, b, h, warp, lane, ids, lo, n, L, ring, bars, o, zacc, sm);
+  else
+    bf16_pages<D, C::kStagesB>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm);
 
   pdl_trigger();
 
@@ -486,10 +581,11 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
     const int c0 = 16 * mt + gid, c1 = c0 + 8;
     float v0 = o[mt][0], v1 = o[mt][1], v2 = o[mt][2], v3 = o[mt][3];
     if (mode == 0) {
-      const float sc = (mt & 1) ? 4194304.f : 16777216.f;   // 2^24 / 4^(mt&1)
+      // undo the code read-out scale: 2^24 / 4^(mt&1), and / 16 for rows gid+8
+      const float sc = (mt & 1) ? 4194304.f : 16777216.f;
       const float za = zz0[mt >> 1], zb = zz1[mt >> 1];
       v0 = fmaf(v0, sc, za); v1 = fmaf(v1, sc, zb);
-      v2 = fmaf(v2, sc, za); v3 = fmaf(v3, sc, zb);
+      v2 = fmaf(v2, sc * 0.0625f, za); v3 = fmaf(v3, sc * 0.0625f, zb);
     }
     wo[(2 * tig) * D + c0] = v0;
     wo[(2 * tig + 1) * D + c0] = v1;
@@ -497,27 +593,33 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
     wo[(2 * tig + 1) * D + c1] = v3;
   }
   __syncthreads();
-  for (int idx = tid; idx < G * D; idx += kDThreads) {
-    const int g = idx / D, ch = idx % D;
+  // per-warp weights 2^(m_w - M) once, then a plain weighted sum per element
+  float* esc = reinterpret_cast<float*>(smem + C::kLps);      // [warps][8] (page list no longer needed)
+  float* gmax = esc + kDWarps * 8;                              // [8]
+  if (tid < kDWarps * 8) {
+    const int w = tid >> 3, g = tid & 7;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, scr[w * (16 + 8 * D) + g]);
-    float Ls = 0.f, Os = 0.f;
-    if (M != -INFINITY) {
+    for (int v = 0; v < kDWarps; ++v) M = fmaxf(M, scr[v * (16 + 8 * D) + g]);
+    const float mw = scr[w * (16 + 8 * D) + g];
+    esc[tid] = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+    if (w == 0) gmax[g] = M;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += kDThreads) {
+    const int g = idx / D, ch = idx % D;
+    float Os = 0.f;
 #pragma unroll
-      for (int w = 0; w < kDWarps; ++w) {
-        const float* base = scr + w * (16 + 8 * D);
-        const float mw = base[g];
-        if (mw != -INFINITY) {
-          const float e = exp2f(mw - M);
-          Ls = fmaf(e, base[8 + g], Ls);
-          Os = fmaf(e, base[16 + g * D + ch], Os);
-        }
-      }
-    }
+    for (int w = 0; w < kDWarps; ++w) Os = fmaf(esc[w * 8 + g], scr[w * (16 + 8 * D) + 16 + g * D + ch], Os);
     float* dst = p.part +
                  ((static_cast<size_t>(b) * p.hq + h * G + g) * p.n_splits + split) * (D + 2);
-    if (ch == 0) { dst[0] = M; dst[1] = Ls; }
+    if (ch == 0) {
+      float Ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDWarps; ++w) Ls = fmaf(esc[w * 8 + g], scr[w * (16 + 8 * D) + 8 + g], Ls);
+      dst[0] = gmax[g];
+      dst[1] = Ls;
+    }
     dst[2 + ch] = Os;
   }
 }
@@ -553,18 +655,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
     }
   }
   pdl_wait();
+  pdl_trigger();
   const int ns = p.n_splits;
   const float* base = p.part + (static_cast<size_t>(b) * p.hq + h * p.G + g) * ns * (D + 2);
+  // every load that does not need the weights is issued in the first round trip
+  constexpr int MAXR = 24;
+  const int ch = tid % D, sg = tid / D;
+  float ov[MAXR];
+#pragma unroll
+  for (int r = 0; r < MAXR; ++r) {
+    const int sp = sg + r * SG;
+    ov[r] = sp < ns ? base[sp * (D + 2) + 2 + ch] : 0.f;
+  }
   if (warp == 0) {
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, base[s * (D + 2)]);
+    float mv[2], lv[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int sp = lane + 32 * r;
+      mv[r] = sp < ns ? base[sp * (D + 2)] : -INFINITY;
+      lv[r] = sp < ns ? base[sp * (D + 2) + 1] : 0.f;
+    }
+    float M = fmaxf(mv[0], mv[1]);
+    for (int sp = lane + 64; sp < ns; sp += 32) M = fmaxf(M, base[sp * (D + 2)]);
     M = warp_max(M);
     float Ls = 0.f;
-    for (int s = lane; s < ns; s += 32) {
-      const float ms = base[s * (D + 2)];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int sp = lane + 32 * r;
+      if (sp < ns) {
+        const float w = (mv[r] == -INFINITY) ? 0.f : exp2f(mv[r] - M);
+        wsplit[sp] = w;
+        Ls = fmaf(w, lv[r], Ls);
+      }
+    }
+    for (int sp = lane + 64; sp < ns; sp += 32) {
+      const float ms = base[sp * (D + 2)];
       const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wsplit[s] = w;
-      Ls = fmaf(w, base[s * (D + 2) + 1], Ls);
+      wsplit[sp] = w;
+      Ls = fmaf(w, base[sp * (D + 2) + 1], Ls);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
@@ -572,13 +700,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
   }
   __syncthreads();
   {
-    const int ch = tid % D, sg = tid / D;
     float ar = 0.f, aw = 0.f;
     const int n_rot = kBf16Only ? 0 : p.n_main;
-#pragma unroll 8
-    for (int s = sg; s < ns; s += SG) {
-      const float v = wsplit[s] * base[s * (D + 2) + 2 + ch];
-      if (s < n_rot) ar += v; else aw += v;
+#pragma unroll
+    for (int r = 0; r < MAXR; ++r) {
+      const int sp = sg + r * SG;
+      if (sp < ns) {
+        const float v = wsplit[sp] * ov[r];
+        if (sp < n_rot) ar += v; else aw += v;
+      }
+    }
+    for (int sp = sg + MAXR * SG; sp < ns; sp += SG) {
+      const float v = wsplit[sp] * base[sp * (D + 2) + 2 + ch];
+      if (sp < n_rot) ar += v; else aw += v;
     }
     acc_rot[sg][ch] = ar;
     acc_raw[sg][ch] = aw;
@@ -669,13 +803,15 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
     return OSCAR_ERR_CUDA;
   const dim3 sgrid(pl.n_splits, p.hkv, p.batch);
   cudaError_t e;
+  // every kernel is launched with programmatic stream serialisation: it may
+  // start while its predecessor drains, and waits (griddepcontrol.wait) before
+  // touching anything the predecessor produces
   if (!kBf16Only) {
-    qrot_kernel<D><<<dim3(p.hkv, p.batch), 1024, 0, st>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_CUDA;
+    e = launch_pdl(qrot_kernel<D>, dim3(p.hkv, p.batch), dim3(1024), 0, st, p);
+    if (e != cudaSuccess) return OSCAR_ERR_CUDA;
     e = launch_pdl(split_kernel<D, kBf16Only>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   } else {
-    split_kernel<D, kBf16Only><<<sgrid, kDThreads, C::kBytes, st>>>(p);
-    e = cudaGetLastError();
+    e = launch_pdl(split_kernel<D, kBf16Only>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   }
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   e = launch_pdl(combine_kernel<D, kBf16Only>, dim3(p.G, p.hkv, p.batch), dim3(256), 0, st, p);
@@ -727,6 +863,7 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.qrot = reinterpret_cast<float*>(ws);
   p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_off);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->head_dim)));
+  p.wait_first = bf16_only ? 1 : 0;   // the INT2 call is gated by qrot_kernel
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->head_dim == 128)
     return bf16_only ? run_decode<128, true>(p, pl, st) : run_decode<128, false>(p, pl, st);

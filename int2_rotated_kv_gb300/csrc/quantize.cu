@@ -94,6 +94,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
     mbar_init(bar, 1);
     fence_mbar_init();
   }
+  // launched with programmatic stream serialisation: inputs are read only after
+  // the predecessor grid has completed; then the next kernel may launch
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   if (tid == 0) {
     mbar_arrive_expect_tx(bar, D * D * 4);
@@ -315,8 +319,17 @@ oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
   const int sms = oscar_host::sm_count();
   const int64_t per_pair = std::max<int64_t>(1, (2LL * sms + 2 * p.hkv - 1) / (2 * p.hkv));
   const dim3 grid(static_cast<unsigned>(std::min<int64_t>(tiles, per_pair)), p.hkv, 2);
-  quantize_kernel<D><<<grid, kQThreads, smem, st>>>(p);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<D>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 QuantParams base_params(const oscar_cache_desc* c) {
