@@ -171,6 +171,39 @@ __device__ __forceinline__ void softmax_tile(Softmax& st, float (&l)[4], float (
   st.l1 += pr[1] + pr[3];
 }
 
+// Same update for two 16-token tiles at once (one vote, one rescale).  The
+// probability sum is accumulated elsewhere (ones row of the zero-term MMA).
+template <int NT>
+__device__ __forceinline__ void softmax_pair(Softmax& st, float (&la)[4], float (&lb)[4],
+                                             float (&o)[NT][4], float (&z)[4], float (&pa)[4],
+                                             float (&pb)[4]) {
+  float mx0 = fmaxf(fmaxf(la[0], la[2]), fmaxf(lb[0], lb[2]));
+  float mx1 = fmaxf(fmaxf(la[1], la[3]), fmaxf(lb[1], lb[3]));
+  if (__any_sync(0xffffffffu, mx0 > st.m0 + kTau || mx1 > st.m1 + kTau)) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
+    const float a0 = (n0 == st.m0) ? 1.f : fast_exp2(st.m0 - n0);
+    const float a1 = (n1 == st.m1) ? 1.f : fast_exp2(st.m1 - n1);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      o[t][0] *= a0; o[t][2] *= a0;
+      o[t][1] *= a1; o[t][3] *= a1;
+    }
+    z[0] *= a0; z[1] *= a1; z[2] *= a0; z[3] *= a1;
+    st.m0 = n0; st.m1 = n1;
+  }
+  const float b0 = st.m0 == -INFINITY ? 0.f : st.m0;
+  const float b1 = st.m1 == -INFINITY ? 0.f : st.m1;
+  pa[0] = fast_exp2(la[0] - b0); pa[1] = fast_exp2(la[1] - b1);
+  pa[2] = fast_exp2(la[2] - b0); pa[3] = fast_exp2(la[3] - b1);
+  pb[0] = fast_exp2(lb[0] - b0); pb[1] = fast_exp2(lb[1] - b1);
+  pb[2] = fast_exp2(lb[2] - b0); pb[3] = fast_exp2(lb[3] - b1);
+}
+
 __device__ __forceinline__ bool tok_ok(int t, int L, int sink, int window, int mode) {
   // mode 0: INT2 region; 1: BF16 region (sink + recent); 2: all tokens
   if (mode == 0) return t >= sink && t < L - window;
@@ -180,14 +213,16 @@ __device__ __forceinline__ bool tok_ok(int t, int L, int sink, int window, int m
 
 // Bounded wait on one stage; a timeout drains the copies still in flight (with
 // the same bound) and reports false so the caller stops.
-template <int NS>
+// kAllIssued: every page of the warp was copied (INT2 rings copy page 0 for an
+// invalid id); otherwise only pages with a valid id were.
+template <int NS, bool kAllIssued = false>
 __device__ __forceinline__ bool wait_stage(uint64_t* wbar, int s, uint32_t& phase, int i, int my_n,
                                            const int* ids, int warp, int32_t* status) {
   const bool ok = mbar_wait(&wbar[s], (phase >> s) & 1u, status);
   phase ^= 1u << s;
   if (__all_sync(0xffffffffu, ok)) return true;
   for (int j = i + 1; j < min(i + NS, my_n); ++j) {
-    if (ids[warp + kDWarps * j] >= 0) {
+    if (kAllIssued || ids[warp + kDWarps * j] >= 0) {
       const int sj = j % NS;
       mbar_wait(&wbar[sj], (phase >> sj) & 1u, status);
       phase ^= 1u << sj;
@@ -196,33 +231,135 @@ __device__ __forceinline__ bool wait_stage(uint64_t* wbar, int s, uint32_t& phas
   return false;
 }
 
+// q.K for one INT2 page-head staged at st: log2-domain logits in the m16n8
+// accumulator layout (rows = tokens gid / gid+8, cols = query heads 2tig / 2tig+1).
+template <int D>
+__device__ __forceinline__ void int2_qk(const uint8_t* st, const uint2* qbs, uint32_t qz, float ks,
+                                        int lane, float (&lg)[4]) {
+  constexpr int NG = D / 32;
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t kw[NG];
+  if constexpr (NG == 4) {
+    const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kKc)[lane];
+    kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
+  } else {
+    const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kKc)[lane];
+    kw[0] = v.x; kw[1] = v.y;
+  }
+  const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kKsz);
+  uint32_t za = 0, zb = 0;
+  if (tig < NG) {
+    const uint32_t e0 = ksz[gid * NG + tig], e1 = ksz[(gid + 8) * NG + tig];
+    za = __byte_perm(e0, e0, 0x3232);
+    zb = __byte_perm(e1, e1, 0x3232);
+  }
+  mma_f16_z(lg, za, zb, 0u, 0u, qz, 0u);          // zero term, already in log2 units
+  uint32_t sa[NG], sb[NG];
+  if constexpr (NG == 4) {
+    const uint4 a = reinterpret_cast<const uint4*>(ksz)[gid];
+    const uint4 c = reinterpret_cast<const uint4*>(ksz)[gid + 8];
+    sa[0] = a.x; sa[1] = a.y; sa[2] = a.z; sa[3] = a.w;
+    sb[0] = c.x; sb[1] = c.y; sb[2] = c.z; sb[3] = c.w;
+  } else {
+    const uint2 a = reinterpret_cast<const uint2*>(ksz)[gid];
+    const uint2 c = reinterpret_cast<const uint2*>(ksz)[gid + 8];
+    sa[0] = a.x; sa[1] = a.y;
+    sb[0] = c.x; sb[1] = c.y;
+  }
+#pragma unroll
+  for (int m = 0; m < NG; ++m) {
+    // pair (s, i) sits at bits 4s+2i (+16); s = 2, 3 are reached with one shift
+    // by 8, so every extracted half is code * 4^i * 16^(s&1) * 2^-24
+    const uint32_t wl = kw[m], wh = kw[m] >> 8;
+    const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
+    const uint2 b0 = qbs[(2 * m) * 32 + lane], b1 = qbs[(2 * m + 1) * 32 + lane];
+    float dg[4];
+    // A registers a0..a3 hold key pairs s = 0, 2, 1, 3
+    mma_f16_z(dg, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
+    mma_f16(dg, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+    const float fa = half_lo(sa[m]) * ks, fb = half_lo(sb[m]) * ks;
+    lg[0] = fmaf(fa, dg[0], lg[0]);
+    lg[1] = fmaf(fa, dg[1], lg[1]);
+    lg[2] = fmaf(fb, dg[2], lg[2]);
+    lg[3] = fmaf(fb, dg[3], lg[3]);
+  }
+}
+
+// p.V for one INT2 page-head: o (channel x query head) += codes^T (p * s), plus
+// the zero term and, on the spare row NG, the probability sum (ones row).
+template <int D>
+__device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4], int lane,
+                                        float (&o)[D / 16][4], float (&zacc)[4]) {
+  constexpr int NG = D / 32;
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0], pr[1]));
+  const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2], pr[3]));
+  uint32_t vw[NG], vs0[NG], vs1[NG];
+  const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVs);
+  if constexpr (NG == 4) {
+    const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kVc)[lane];
+    vw[0] = v.x; vw[1] = v.y; vw[2] = v.z; vw[3] = v.w;
+    const uint4 a = reinterpret_cast<const uint4*>(vsw)[tig * 2];
+    const uint4 c = reinterpret_cast<const uint4*>(vsw)[tig * 2 + 1];
+    vs0[0] = a.x; vs0[1] = a.y; vs0[2] = a.z; vs0[3] = a.w;
+    vs1[0] = c.x; vs1[1] = c.y; vs1[2] = c.z; vs1[3] = c.w;
+  } else {
+    const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kVc)[lane];
+    vw[0] = v.x; vw[1] = v.y;
+    const uint2 a = reinterpret_cast<const uint2*>(vsw)[tig * 2];
+    const uint2 c = reinterpret_cast<const uint2*>(vsw)[tig * 2 + 1];
+    vs0[0] = a.x; vs0[1] = a.y;
+    vs1[0] = c.x; vs1[1] = c.y;
+  }
+#pragma unroll
+  for (int m = 0; m < NG; ++m) {
+    const uint32_t bb0 = hmul2_u32(pb0, vs0[m]);
+    const uint32_t bb1 = hmul2_u32(pb1, vs1[m]);
+    // value pair s = r: rows gid (s = 0, 2) read at 4^i, rows gid+8 (s = 1, 3) at 16 * 4^i
+    const uint32_t wl = vw[m], wh = vw[m] >> 8;
+    const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
+    mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bb0, bb1);
+    mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
+            bb0, bb1);
+  }
+  const uint32_t* vz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVz);
+  uint32_t za0 = 0, za2 = 0;
+  if (gid < NG) {
+    za0 = vz[(tig * 2) * NG + gid];
+    za2 = vz[(tig * 2 + 1) * NG + gid];
+  } else if (gid == NG) {
+    za0 = za2 = 0x3C003C00u;   // ones: row NG accumulates sum_t p
+  }
+  mma_f16(zacc, za0, 0u, za2, 0u, pb0, pb1);
+}
+
 // INT2 pages [lo, lo + n) of one (sequence, KV head): warp w takes pages
-// w, w + 8, ... through its own ring of NS bulk-copied page-head blocks.
+// w, w + 8, ... through its own ring of NS bulk-copied page-head blocks, two
+// pages per step so their dependency chains overlap and share one softmax
+// update.  Invalid page ids (negative) copy page 0 and are masked out.
 template <int D, int NS>
 __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, int lo, int n, int L, uint8_t* ring,
-                                           uint64_t* bars, float (&o)[D / 16][4], float (&zacc)[4],
-                                           Softmax& sm) {
+                                           uint64_t* bars, uint2* qbs, float (&o)[D / 16][4],
+                                           float (&zacc)[4], Softmax& sm) {
+  static_assert(NS % 2 == 0, "pages are consumed in pairs of stages");
   constexpr int NG = D / 32, NK = D / 16;
   constexpr int SB = Fmt<D>::kInt2Block;
   const int gid = lane >> 2, tig = lane & 3, G = p.G;
   uint8_t* wring = ring + warp * NS * SB;
-  uint64_t* wbar = reinterpret_cast<uint64_t*>(bars) + warp * 8;
+  uint64_t* wbar = bars + warp * 8;
   const uint8_t* pool_h = p.int2_pool + static_cast<size_t>(h) * SB;
   const size_t pstride = static_cast<size_t>(p.hkv) * SB;
   const int my_n = n > warp ? (n - warp + kDWarps - 1) / kDWarps : 0;
+  const int* wids = ids + warp;                   // page i of this warp: wids[8 i]
   if (lane == 0) {
     for (int i = 0; i < min(NS, my_n); ++i) {
-      const int id = ids[warp + kDWarps * i];
-      if (id >= 0) {
-        mbar_arrive_expect_tx(&wbar[i], SB);
-        bulk_g2s(wring + i * SB, pool_h + id * pstride, SB, &wbar[i]);
-      }
+      mbar_arrive_expect_tx(&wbar[i], SB);
+      bulk_g2s(wring + i * SB, pool_h + max(wids[kDWarps * i], 0) * pstride, SB, &wbar[i]);
     }
   }
-  // ---- query operand, once the rotated query is complete
+  // ---- query operand, once the rotated query is complete (warp 0 stages it)
   pdl_wait();
-  uint32_t qb[NK][2];
   uint32_t qz = 0;
   {
     const float* qr = p.qrot + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
@@ -237,10 +374,12 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
         v1 = *reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig + 8);
       }
       gs[kk >> 1] += (v0.x + v0.y) + (v1.x + v1.y);
-      // codes of k-step parity i and channel half h are read at 4^i * 16^h
-      const float sc = (kk & 1) ? 0.25f : 1.f;
-      qb[kk][0] = pack_half2(v0.x * sc, v0.y * sc);
-      qb[kk][1] = pack_half2(v1.x * sc * 0.0625f, v1.y * sc * 0.0625f);
+      if (warp == 0) {
+        // codes of k-step parity i and channel half h are read at 4^i * 16^h
+        const float sc = (kk & 1) ? 0.25f : 1.f;
+        qbs[kk * 32 + lane] = make_uint2(pack_half2(v0.x * sc, v0.y * sc),
+                                         pack_half2(v1.x * sc * 0.0625f, v1.y * sc * 0.0625f));
+      }
     }
     float mine = 0.f;
 #pragma unroll
@@ -257,124 +396,61 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
            (static_cast<uint32_t>(__half_as_ushort(lo16)) << 16);
     }
   }
+  __syncthreads();
   const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
   const int tok_lo = p.sink, tok_hi = L - p.window;
   uint32_t phase = 0;
   int s = 0;
-  for (int i = 0; i < my_n; ++i) {
-    const int k = warp + kDWarps * i;
-    if (ids[k] >= 0) {
-      if (!wait_stage<NS>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
-      const uint8_t* st = wring + s * SB;
-      // ---- q.K over exact 2-bit codes, one accumulator per group
-      uint32_t kw[NG];
-      if constexpr (NG == 4) {
-        const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kKc)[lane];
-        kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
-      } else {
-        const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kKc)[lane];
-        kw[0] = v.x; kw[1] = v.y;
-      }
-      float dg[NG][4];
-#pragma unroll
-      for (int m = 0; m < NG; ++m) {
-        // pair (s, i) sits at bits 4s+2i (+16); s = 2, 3 are reached with one
-        // shift by 8, so every extracted half is code * 4^i * 16^(s&1) * 2^-24
-        const uint32_t wl = kw[m], wh = kw[m] >> 8;
-        const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
-        // A registers a0..a3 hold key pairs s = 0, 2, 1, 3
-        mma_f16_z(dg[m], wl & m0, wh & m0, wl & m1, wh & m1, qb[2 * m][0], qb[2 * m][1]);
-        mma_f16(dg[m], wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2),
-                qb[2 * m + 1][0], qb[2 * m + 1][1]);
-      }
-      const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kKsz);
-      uint32_t za = 0, zb = 0;
-      if (tig < NG) {
-        const uint32_t e0 = ksz[gid * NG + tig], e1 = ksz[(gid + 8) * NG + tig];
-        za = __byte_perm(e0, e0, 0x3232);
-        zb = __byte_perm(e1, e1, 0x3232);
-      }
-      float lg[4];
-      mma_f16_z(lg, za, zb, 0u, 0u, qz, 0u);       // zero term, already in log2 units
-      uint32_t sa[NG], sb[NG];
-      if constexpr (NG == 4) {
-        const uint4 a = reinterpret_cast<const uint4*>(ksz)[gid];
-        const uint4 c = reinterpret_cast<const uint4*>(ksz)[gid + 8];
-        sa[0] = a.x; sa[1] = a.y; sa[2] = a.z; sa[3] = a.w;
-        sb[0] = c.x; sb[1] = c.y; sb[2] = c.z; sb[3] = c.w;
-      } else {
-        const uint2 a = reinterpret_cast<const uint2*>(ksz)[gid];
-        const uint2 c = reinterpret_cast<const uint2*>(ksz)[gid + 8];
-        sa[0] = a.x; sa[1] = a.y;
-        sb[0] = c.x; sb[1] = c.y;
-      }
-#pragma unroll
-      for (int m = 0; m < NG; ++m) {
-        const float fa = half_lo(sa[m]) * ks, fb = half_lo(sb[m]) * ks;
-        lg[0] = fmaf(fa, dg[m][0], lg[0]);
-        lg[1] = fmaf(fa, dg[m][1], lg[1]);
-        lg[2] = fmaf(fb, dg[m][2], lg[2]);
-        lg[3] = fmaf(fb, dg[m][3], lg[3]);
-      }
-      // tokens outside [sink, L - window) only occur on the range's end pages
-      const int pbeg = (lo + k) * kPage;
-      if (pbeg < tok_lo || pbeg + kPage > tok_hi) {
-        const int t0 = pbeg + gid, t1 = t0 + 8;
-        if (t0 < tok_lo || t0 >= tok_hi) lg[0] = lg[1] = -INFINITY;
-        if (t1 < tok_lo || t1 >= tok_hi) lg[2] = lg[3] = -INFINITY;
-      }
-      float pr[4];
-      softmax_tile<NK>(sm, lg, o, zacc, pr);
-      // ---- p.V over exact 2-bit codes, p * s per group as the B operand
-      const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0], pr[1]));
-      const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2], pr[3]));
-      uint32_t vw[NG], vs0[NG], vs1[NG];
-      const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVs);
-      if constexpr (NG == 4) {
-        const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kVc)[lane];
-        vw[0] = v.x; vw[1] = v.y; vw[2] = v.z; vw[3] = v.w;
-        const uint4 a = reinterpret_cast<const uint4*>(vsw)[tig * 2];
-        const uint4 c = reinterpret_cast<const uint4*>(vsw)[tig * 2 + 1];
-        vs0[0] = a.x; vs0[1] = a.y; vs0[2] = a.z; vs0[3] = a.w;
-        vs1[0] = c.x; vs1[1] = c.y; vs1[2] = c.z; vs1[3] = c.w;
-      } else {
-        const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kVc)[lane];
-        vw[0] = v.x; vw[1] = v.y;
-        const uint2 a = reinterpret_cast<const uint2*>(vsw)[tig * 2];
-        const uint2 c = reinterpret_cast<const uint2*>(vsw)[tig * 2 + 1];
-        vs0[0] = a.x; vs0[1] = a.y;
-        vs1[0] = c.x; vs1[1] = c.y;
-      }
-#pragma unroll
-      for (int m = 0; m < NG; ++m) {
-        const uint32_t bb0 = hmul2_u32(pb0, vs0[m]);
-        const uint32_t bb1 = hmul2_u32(pb1, vs1[m]);
-        // value pair s = r: rows gid (s = 0, 2) read at 4^i, rows gid+8 (s = 1, 3) at 16 * 4^i
-        const uint32_t wl = vw[m], wh = vw[m] >> 8;
-        const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
-        mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bb0, bb1);
-        mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
-                bb0, bb1);
-      }
-      const uint32_t* vz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVz);
-      uint32_t za0 = 0, za2 = 0;
-      if (gid < NG) {
-        za0 = vz[(tig * 2) * NG + gid];
-        za2 = vz[(tig * 2 + 1) * NG + gid];
-      }
-      mma_f16(zacc, za0, 0u, za2, 0u, pb0, pb1);
+  int i = 0;
+  for (; i + 1 < my_n; i += 2) {
+    const int idA = wids[kDWarps * i], idB = wids[kDWarps * (i + 1)];
+    if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
+    if (!wait_stage<NS, true>(wbar, s + 1, phase, i + 1, my_n, ids, warp, p.status)) return;
+    const uint8_t* stA = wring + s * SB;
+    const uint8_t* stB = stA + SB;
+    float la[4], lb[4];
+    int2_qk<D>(stA, qbs, qz, ks, lane, la);
+    int2_qk<D>(stB, qbs, qz, ks, lane, lb);
+    const int pA = (lo + warp + kDWarps * i) * kPage, pB = pA + kDWarps * kPage;
+    if (pA < tok_lo || pB + kPage > tok_hi || (idA | idB) < 0) {
+      const int t0 = pA + gid, t1 = t0 + 8, u0 = pB + gid, u1 = u0 + 8;
+      if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
+      if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
+      if (idB < 0 || u0 < tok_lo || u0 >= tok_hi) lb[0] = lb[1] = -INFINITY;
+      if (idB < 0 || u1 < tok_lo || u1 >= tok_hi) lb[2] = lb[3] = -INFINITY;
     }
-    // refill this stage once every lane is done reading it (the warp barrier
-    // orders the reads before the bulk copy that overwrites the stage)
+    float pa[4], pbv[4];
+    softmax_pair<NK>(sm, la, lb, o, zacc, pa, pbv);
+    int2_pv<D>(stA, pa, lane, o, zacc);
+    int2_pv<D>(stB, pbv, lane, o, zacc);
     __syncwarp();
-    if (lane == 0 && i + NS < my_n) {
-      const int id = ids[k + kDWarps * NS];
-      if (id >= 0) {
+    if (lane == 0) {
+      if (i + NS < my_n) {
         mbar_arrive_expect_tx(&wbar[s], SB);
-        bulk_g2s(wring + s * SB, pool_h + id * pstride, SB, &wbar[s]);
+        bulk_g2s(wring + s * SB, pool_h + max(wids[kDWarps * (i + NS)], 0) * pstride, SB, &wbar[s]);
+      }
+      if (i + 1 + NS < my_n) {
+        mbar_arrive_expect_tx(&wbar[s + 1], SB);
+        bulk_g2s(wring + (s + 1) * SB, pool_h + max(wids[kDWarps * (i + 1 + NS)], 0) * pstride,
+                 SB, &wbar[s + 1]);
       }
     }
-    s = (s + 1 == NS) ? 0 : s + 1;
+    s = (s + 2 == NS) ? 0 : s + 2;
+  }
+  if (i < my_n) {   // odd tail: one page
+    const int idA = wids[kDWarps * i];
+    if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
+    const uint8_t* stA = wring + s * SB;
+    float la[4];
+    int2_qk<D>(stA, qbs, qz, ks, lane, la);
+    const int pA = (lo + warp + kDWarps * i) * kPage;
+    const int t0 = pA + gid, t1 = t0 + 8;
+    if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
+    if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
+    float pa[4];
+    float dummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, pd[4];
+    softmax_pair<NK>(sm, la, dummy, o, zacc, pa, pd);
+    int2_pv<D>(stA, pa, lane, o, zacc);
   }
 }
 
@@ -548,7 +624,8 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   float zacc[4] = {0.f, 0.f, 0.f, 0.f};
   Softmax sm{-INFINITY, -INFINITY, 0.f, 0.f};
   if (mode == 0)
-    int2_pages<D, C::kStagesI>(p, b, h, warp, lane, ids, lo, n, L, ring, bars, o, zacc, sm);
+    int2_pages<D, C::kStagesI>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
+                               reinterpret_cast<uint2*>(lps), o, zacc, sm);
   else
     bf16_pages<D, C::kStagesB>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm);
 
@@ -556,10 +633,16 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
 
   // ---- warp result -> shared scratch (the ring is idle once every warp is here)
   float l0 = sm.l0, l1 = sm.l1;
+  if (mode == 0) {
+    // INT2 pages: the probability sum sits on row NG of the zero-term accumulator
+    l0 = __shfl_sync(0xffffffffu, zacc[0], NG * 4 + tig);
+    l1 = __shfl_sync(0xffffffffu, zacc[1], NG * 4 + tig);
+  } else {
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
   }
   float zz0[NG], zz1[NG];
 #pragma unroll

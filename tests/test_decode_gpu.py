@@ -124,3 +124,30 @@ def test_bad_lengths_are_reported_not_faulted():
     ref = attention.mixed_decode(inst.q[:1], inst.k[:1], inst.v[:1], [300], rot, sink=4, window=64,
                                  gqa=4)
     H.check_close(H.from_bf16(o)[:1], ref)
+
+
+def test_bad_page_id_is_masked_and_reported():
+    """An INT2 page id beyond the pool is skipped (its tokens drop out of the
+    softmax) and reported; the other tokens are attended as usual."""
+    t = H.torch()
+    wl = synth.QWEN3_8B_32K
+    inst = synth.draw_instance(wl, n_calib=256, seq_lens=[2500])
+    rot = H.oracle_rotations(inst)
+    cache, pp = H.make_cache(inst, rot, window=128)
+    H.prefill(cache, inst)
+    bad_page = 37
+    tbl = pp.int2_table.copy()
+    tbl[0, bad_page] = pp.num_int2_pages + 3
+    cache.int2_page_table = t.from_numpy(tbl).to(H.DEV)
+    out = H.decode(cache, inst.q, inst.seq_lens)
+    assert H.status(cache) & H.lib().DEVERR_PAGE_ID
+    keep = np.ones(2500, bool)
+    keep[16 * bad_page:16 * bad_page + 16] = False
+    ref = np.zeros_like(out)
+    for h in range(wl.num_kv_heads):
+        ke, ve = attention.effective_kv(inst.k[0][h], inst.v[0][h], 2500, 4, 128, rot.rk[h],
+                                        rot.rv[h], rot.ck[h], rot.cv[h])
+        G = wl.gqa
+        ref[0, h * G:(h + 1) * G] = attention.softmax_attention(inst.q[0, h * G:(h + 1) * G],
+                                                                ke[keep], ve[keep])
+    H.check_close(out, ref)
