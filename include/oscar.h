@@ -181,6 +181,27 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
                                          int32_t max_seq_len, void* out, void* workspace,
                                          size_t workspace_bytes, void* stream);
 
+/* oscar_decode_attention for callers that cannot allocate device memory.
+ * The pages describe no counterpart; it exists because some callers have no
+ * allocator at hand when they run attention: a plug-in inside a runtime that
+ * owns every device allocation, or a latency-bound loop that must never enter
+ * the allocator (which may synchronise or fail under memory pressure).  Instead
+ * of a workspace argument the call uses one 16 MiB scratch buffer compiled into
+ * the library; every GPU that loads the library reserves it until the process
+ * exits.  Shapes whose workspace (oscar_decode_workspace_size) exceeds it return
+ * OSCAR_ERR_WORKSPACE before any launch.  The call allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library routine); the buffer needs no
+ * initial contents, since every call writes each byte it later reads.  All
+ * calls share the one buffer: calls whose kernels overlap on the GPU (streams
+ * without ordering between them, or several host threads) race and give wrong
+ * results -- serialise them.  The first call on a device looks up the buffer's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Other arguments as
+ * oscar_decode_attention. */
+oscar_status oscar_decode_attention_static(const oscar_cache_desc* desc, const void* q,
+                                           const int32_t* seq_lens, int32_t batch,
+                                           int32_t max_seq_len, void* out, void* stream);
+
 /* Number of SMs the split heuristics assume for the current device (>= 1). */
 int32_t oscar_device_sm_count(void);
 

@@ -24,7 +24,7 @@ VARIANT_OSCAR, VARIANT_HADAMARD, VARIANT_IDENTITY = 0, 1, 2
 EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rotation",
             "oscar_prefill_quantize", "oscar_quantize_append", "oscar_decode_workspace_size",
             "oscar_decode_attention", "oscar_decode_attention_bf16", "oscar_device_sm_count",
-            "oscar_status_string", "oscar_version")
+            "oscar_status_string", "oscar_version", "oscar_decode_attention_static")
 
 
 class OscarError(RuntimeError):
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "oscar_decode_attention": (I32, [P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_decode_attention_bf16": (I32, [P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_device_sm_count": (I32, []),
+            "oscar_decode_attention_static": (I32, [P, P, P, I32, I32, P, P]),
             "oscar_status_string": (ctypes.c_char_p, [I32]),
             "oscar_version": (I32, []),
         }
@@ -224,6 +225,17 @@ def oscar_decode_attention_bf16(cache: Cache, q, seq_lens, max_seq_len: int, out
                                              _ptr(workspace),
                                              workspace.numel() * workspace.element_size(),
                                              _stream(stream)))
+
+
+def oscar_decode_attention_static(cache: Cache, q, seq_lens, max_seq_len: int, out, stream=None):
+    """Decode attention without a workspace argument, for callers that cannot
+    allocate device memory: the library's own fixed 16 MiB scratch buffer is
+    used and nothing is allocated.  Calls must not overlap on the GPU."""
+    d = cache.desc()
+    _check("oscar_decode_attention_static",
+           lib().oscar_decode_attention_static(ctypes.byref(d), _ptr(q), _ptr(seq_lens),
+                                               int(seq_lens.numel()), int(max_seq_len), _ptr(out),
+                                               _stream(stream)))
 
 
 def oscar_device_sm_count() -> int:

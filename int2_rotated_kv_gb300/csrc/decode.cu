@@ -985,6 +985,39 @@ bool allow_smem(const void* func, int bytes) {
 
 }  // namespace oscar_host
 
+// ------------------------------------------------ workspace without allocation
+//
+// Some callers cannot allocate device memory at the moment they need attention:
+// plug-ins hosted by a runtime that owns every allocation, or latency-bound
+// loops that must never enter the allocator (it may synchronise, or fail under
+// memory pressure).  For them the library carries one fixed scratch buffer in
+// its own image.  Every GPU that loads the library reserves it until the
+// process exits.
+static __device__ __align__(256) unsigned char g_decode_scratch[size_t(16) << 20];   // 16 MiB
+
+namespace oscar {
+
+constexpr size_t kStaticScratchBytes = sizeof(g_decode_scratch);
+
+// Device address of the scratch buffer on the current device.  In host code the
+// symbol is only a handle; cudaGetSymbolAddress, called once per device with
+// that device current, yields the address the kernels are given.
+void* decode_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return nullptr;
+    addr[dev] = ptr;
+  }
+  return addr[dev];
+}
+
+}  // namespace oscar
+
 extern "C" {
 
 size_t oscar_decode_workspace_size(const oscar_cache_desc* desc, int32_t batch, int32_t max_seq_len) {
@@ -1012,5 +1045,23 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
 }
 
 int32_t oscar_device_sm_count(void) { return oscar_host::sm_count(); }
+
+oscar_status oscar_decode_attention_static(const oscar_cache_desc* desc, const void* q,
+                                           const int32_t* seq_lens, int32_t batch,
+                                           int32_t max_seq_len, void* out, void* stream) {
+  oscar_status st = oscar_host::check_desc(desc, true, true);
+  if (st != OSCAR_OK) return st;
+  if (batch < 0 || max_seq_len < 1) return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return OSCAR_OK;
+  // the same plan the workspace call makes; refuse it if it needs more scratch
+  const oscar::Plan pl = oscar::make_plan(desc, batch, max_seq_len, false);
+  if (pl.total > oscar::kStaticScratchBytes) return OSCAR_ERR_WORKSPACE;
+  void* ws = oscar::decode_scratch_address();
+  if (!ws) return OSCAR_ERR_CUDA;
+  // every byte the kernels read from the scratch is written earlier in the same
+  // call (rotated queries, one partial per split), so nothing is cleared
+  return oscar::decode_entry(desc, q, seq_lens, batch, max_seq_len, out, ws,
+                             oscar::kStaticScratchBytes, stream, false);
+}
 
 }  // extern "C"
