@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
     ap.add_argument("--workload", default=synth.QWEN3_8B_32K.name, choices=list(synth.WORKLOADS))
-    ap.add_argument("--extras", action="store_true", help="also time the 128k, prefix and budget configs")
+    ap.add_argument("--extras", action="store_true",
+                    help="also time the 128k, prefix-sharing and 40 GB budget workloads (append, prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-calib", type=int, default=None)
     ap.add_argument("--profile", action="store_true",
@@ -194,22 +195,26 @@ def bf16_dev(a, dev):
         torch.bfloat16).to(dev)
 
 
-def prefill_layer(cache, inst, lens, dev):
+def device_inputs(inst, dev):
+    """A host-drawn Instance in the DeviceInstance layout: prefill lists of
+    tokens [0, L_b - 1), the new token L_b - 1 and the decode query."""
     import torch
-    from int2_rotated_kv_gb300 import _lib as L
     H = inst.workload.num_kv_heads
+    lens = np.asarray(inst.seq_lens, np.int64)
     ks, vs, sid, pos = [], [], [], []
-    for b, n in enumerate(lens):
-        n = int(n)
+    for b, L in enumerate(lens):
+        n = int(L) - 1
         ks.append(np.stack([inst.k[b][h][:n] for h in range(H)], 1))
         vs.append(np.stack([inst.v[b][h][:n] for h in range(H)], 1))
         sid.append(np.full(n, b, np.int32))
         pos.append(np.arange(n, dtype=np.int32))
-    L.oscar_prefill_quantize(cache, bf16_dev(np.concatenate(ks), dev), bf16_dev(np.concatenate(vs), dev),
-                             torch.from_numpy(np.concatenate(sid)).to(dev),
-                             torch.from_numpy(np.concatenate(pos)).to(dev),
-                             torch.tensor(np.asarray(lens, np.int32), device=dev))
-    torch.cuda.synchronize()
+    kn = np.stack([[inst.k[b][h][int(lens[b]) - 1] for h in range(H)] for b in range(len(lens))])
+    vn = np.stack([[inst.v[b][h][int(lens[b]) - 1] for h in range(H)] for b in range(len(lens))])
+    return synth.DeviceInstance(
+        inst.workload, inst.params, inst.calib_q, inst.calib_k, inst.calib_v, lens,
+        bf16_dev(np.concatenate(ks), dev), bf16_dev(np.concatenate(vs), dev),
+        torch.from_numpy(np.concatenate(sid)).to(dev), torch.from_numpy(np.concatenate(pos)).to(dev),
+        bf16_dev(kn, dev), bf16_dev(vn, dev), bf16_dev(inst.q, dev))
 
 
 def clone_cache(c):
@@ -220,10 +225,11 @@ def clone_cache(c):
 class Decoder:
     """One set of layer caches plus the per-step calls (INT2 mixed or BF16-only)."""
 
-    def __init__(self, inst, lens_final, rot, dev, *, bf16_only=False, l2_bytes=0):
+    def __init__(self, di, rot, dev, *, bf16_only=False, l2_bytes=0):
         import torch
         from int2_rotated_kv_gb300 import _lib as L
-        w = inst.workload
+        w = di.workload
+        lens_final = di.seq_lens
         self.L, self.torch, self.dev = L, torch, dev
         self.w, self.bf16_only = w, bf16_only
         self.S = w.sink
@@ -238,7 +244,9 @@ class Decoder:
         rk, rv, ck, cv = rot
         base = pages.allocate(pp, hkv=hkv, hq=hq, d=d, sink=self.S, window=self.W, device=dev,
                               r_k=rk, r_v=rv, clip_k=ck, clip_v=cv)
-        prefill_layer(base, inst, self.lens - 1, dev)
+        L.oscar_prefill_quantize(base, di.k_tok, di.v_tok, di.seq_ids, di.positions,
+                                 torch.tensor((self.lens - 1).astype(np.int32), device=dev))
+        torch.cuda.synchronize()
         self.layer_bytes = (base.int2_pool.numel() + base.bf16_pool.numel() * 2)
         self.step_bytes = attention_bytes(self.lens, hkv, hq, d, self.S, self.W, bf16_only)
         self.attn_bytes = self.step_bytes
@@ -246,10 +254,7 @@ class Decoder:
         touched = attention_bytes(self.lens, hkv, hq, d, self.S, self.W, bf16_only)
         n_layers = max(2, math.ceil(3 * l2_bytes / max(touched, 1)) + 1) if l2_bytes else 1
         self.caches = [base] + [clone_cache(base) for _ in range(n_layers - 1)]
-        kn = np.stack([[inst.k[b][h][int(self.lens[b]) - 1] for h in range(hkv)] for b in range(B)])
-        vn = np.stack([[inst.v[b][h][int(self.lens[b]) - 1] for h in range(hkv)] for b in range(B)])
-        self.k_new, self.v_new = bf16_dev(kn, dev), bf16_dev(vn, dev)
-        self.q = bf16_dev(inst.q, dev)
+        self.k_new, self.v_new, self.q = di.k_new, di.v_new, di.q
         self.lens_dev = torch.tensor(self.lens.astype(np.int32), device=dev)
         self.max_len = int(self.lens.max())
         self.out = torch.zeros((B, hq, d), dtype=torch.bfloat16, device=dev)
@@ -316,6 +321,35 @@ def time_steps(dec, steps, warmup, chunk=64, clocks=None, barrier=None):
     if barrier:
         barrier()
     return e0.elapsed_time(e1) / steps, clk
+
+
+def time_graph(dec, fn, steps, warmup, chunk=64):
+    """Device time of fn(i) (one call per layer index), replayed from CUDA graphs."""
+    torch = dec.torch
+    chunk = max(dec.n_layers, (chunk // dec.n_layers) * dec.n_layers)
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn(0)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for i in range(chunk):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // chunk)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * chunk)
 
 
 def time_decode_calls(dec, iters=200, batch=40):
@@ -461,30 +495,140 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------- extras
 
-def extra_decode(name, dev, l2, n_calib, steps=200, warmup=10):
-    """µs/layer and GB/s for another workload (INT2 and BF16 at the same batch)."""
+def decode_leg(di, rot, dev, l2, steps=200, warmup=10, bf16_only=False):
+    """One layer's decode step (append + attention) at di's shape: µs, GB/s,
+    and the decode call alone."""
     torch = __import__("torch")
-    w = synth.WORKLOADS[name]
-    inst = synth.draw_instance(w, n_calib=n_calib)
-    rot = calibrate_with_library(inst, n_calib)
-    dec = Decoder(inst, inst.seq_lens, rot, dev, l2_bytes=l2)
-    t, _ = time_steps(dec, steps, warmup)
-    med, _ = time_decode_calls(dec, 100)
-    res = {"us_per_layer_step": round(t * 1e3, 3), "GBps": round(dec.step_bytes / t / 1e6, 1),
-           "decode_call_us": round(med * 1e3, 3),
+    dec = Decoder(di, rot, dev, bf16_only=bf16_only, l2_bytes=l2)
+    t, clk = time_steps(dec, steps, warmup, clocks=Clocks(torch.cuda.current_device()))
+    med, mean = time_decode_calls(dec, 100)
+    res = {"batch": len(di.seq_lens), "us_per_layer_step": round(t * 1e3, 3),
+           "GBps": round(dec.step_bytes / t / 1e6, 1), "decode_call_us": round(med * 1e3, 3),
            "decode_call_GBps": round(dec.attn_bytes / med / 1e6, 1),
-           "batch": len(inst.seq_lens), "layers_rotated": dec.n_layers}
+           "algorithmic_bytes_per_step": int(dec.step_bytes), "layers_rotated": dec.n_layers,
+           "cache_bytes_per_layer": int(dec.layer_bytes), "clocks": clk}
     del dec
     torch.cuda.empty_cache()
-    try:
-        decb = Decoder(inst, inst.seq_lens, rot, dev, bf16_only=True, l2_bytes=l2)
-        tb, _ = time_steps(decb, steps, warmup)
-        res["bf16_us_per_layer_step"] = round(tb * 1e3, 3)
-        res["bf16_GBps"] = round(decb.step_bytes / tb / 1e6, 1)
-        res["speedup_vs_bf16"] = round(tb / t, 3)
-        del decb
-    except Exception as e:   # out of memory for the BF16 copy of a very long context
-        res["bf16_error"] = str(e)[:120]
+    return res
+
+
+def extra_long(dev, l2, n_calib):
+    """Qwen3-32B shape, one 131072-token sequence: INT2 and BF16 at batch 1."""
+    w = synth.QWEN3_32B_128K
+    di = synth.draw_device(w, w.seq_lens(), dev, n_calib=n_calib)
+    rot = calibrate_with_library(di, n_calib)
+    res = decode_leg(di, rot, dev, l2)
+    bf = decode_leg(di, rot, dev, l2, bf16_only=True)
+    res["bf16"] = bf
+    res["speedup_vs_bf16"] = round(bf["us_per_layer_step"] / res["us_per_layer_step"], 3)
+    return res
+
+
+def extra_prefix(dev, l2, n_calib):
+    """Qwen3-4B shape, 64 sequences of U{4096..8192} tokens sharing a 2048-token
+    prefix (128 pages per sequence with equal page ids).  GB/s on unique bytes:
+    the shared pages count once."""
+    w = synth.QWEN3_4B_PREFIX
+    lens = w.seq_lens()
+    di = synth.draw_device(w, lens, dev, n_calib=n_calib)
+    rot = calibrate_with_library(di, n_calib)
+    res = decode_leg(di, rot, dev, l2)
+    i2, bfb = token_bytes(w.head_dim)
+    P, B, H = w.shared_prefix, len(lens), w.num_kv_heads
+    shared_int2 = H * (w.sink * bfb + (P - w.sink) * i2)
+    shared_bf16 = H * P * bfb
+    res["unique_GBps"] = round((res["algorithmic_bytes_per_step"] - (B - 1) * shared_int2) /
+                               res["us_per_layer_step"] / 1e3, 1)
+    bf = decode_leg(di, rot, dev, l2, bf16_only=True)
+    bf["unique_GBps"] = round((bf["algorithmic_bytes_per_step"] - (B - 1) * shared_bf16) /
+                              bf["us_per_layer_step"] / 1e3, 1)
+    res["bf16"] = bf
+    res["speedup_vs_bf16"] = round(bf["us_per_layer_step"] / res["us_per_layer_step"], 3)
+    res["seq_lens"] = {"min": int(lens.min()), "max": int(lens.max()), "sum": int(lens.sum())}
+    return res
+
+
+def pool_bytes_per_seq(w, L, bf16_only):
+    """Allocated page-slot bytes of one sequence of L tokens in one layer (the
+    same page plan the decoder allocates: cache filled to L - 1 plus one page of growth)."""
+    S, W = (0, L + 1) if bf16_only else (w.sink, w.window)
+    pp = pages.plan(np.array([L - 1]), S, W, growth=1)
+    d, H = w.head_dim, w.num_kv_heads
+    return pp.num_int2_pages * H * 12 * d + pp.num_bf16_pages * H * 64 * d
+
+
+def extra_budget(dev, l2, n_calib, budget=40e9):
+    """Qwen3-8B shape at L = 4096 under a 40e9-byte cache budget over 36 layers:
+    the INT2 and BF16 batches that fit, one layer timed (tokens/s = batch /
+    (36 t_layer), attention only); INT2 also at the BF16 batch; the append at
+    batch 256 alone; the bulk prefill of 256 x 4096 tokens."""
+    torch = __import__("torch")
+    from int2_rotated_kv_gb300 import _lib as L
+    w = synth.QWEN3_8B_BUDGET
+    Lc, layers = int(w.context), w.layers
+    per_i2 = pool_bytes_per_seq(w, Lc, False) * layers
+    per_bf = pool_bytes_per_seq(w, Lc, True) * layers
+    b_i2, b_bf = int(budget // per_i2), int(budget // per_bf)
+    res = {"budget_bytes": budget, "layers": layers, "int2_bytes_per_seq": per_i2,
+           "bf16_bytes_per_seq": per_bf, "int2_batch": b_i2, "bf16_batch": b_bf}
+    di = synth.draw_device(w, np.full(b_i2, Lc), dev, n_calib=n_calib)
+    rot = calibrate_with_library(di, n_calib)
+    r = decode_leg(di, rot, dev, l2, steps=100, warmup=5)
+    r["tokens_per_s"] = round(b_i2 / (layers * r["us_per_layer_step"] * 1e-6), 1)
+    res["int2_at_budget"] = r
+    del di
+    di = synth.draw_device(w, np.full(b_bf, Lc), dev, n_calib=n_calib)
+    r = decode_leg(di, rot, dev, l2, steps=100, warmup=5, bf16_only=True)
+    r["tokens_per_s"] = round(b_bf / (layers * r["us_per_layer_step"] * 1e-6), 1)
+    res["bf16_at_budget"] = r
+    r = decode_leg(di, rot, dev, l2, steps=100, warmup=5)
+    r["tokens_per_s"] = round(b_bf / (layers * r["us_per_layer_step"] * 1e-6), 1)
+    res["int2_at_bf16_batch"] = r
+    res["tokens_per_s_ratio_at_equal_memory"] = round(
+        res["int2_at_budget"]["tokens_per_s"] / res["bf16_at_budget"]["tokens_per_s"], 3)
+    del di
+    torch.cuda.empty_cache()
+    # append alone at batch 256 (graph-replayed, rotating layer caches)
+    di = synth.draw_device(w, np.full(256, Lc), dev, n_calib=n_calib)
+    dec = Decoder(di, rot, dev, l2_bytes=l2)
+    t = time_graph(dec, dec.append, 400, 10)
+    nb = append_bytes(dec.lens, w.num_kv_heads, w.head_dim, w.sink, w.window)
+    res["append_b256"] = {"us": round(t * 1e3, 3), "GBps": round(nb / t / 1e6, 1),
+                          "algorithmic_bytes": int(nb)}
+    del dec, di
+    torch.cuda.empty_cache()
+    # bulk prefill: 256 sequences x 4096 tokens placed in one call
+    di = synth.draw_device(w, np.full(256, Lc + 1), dev, n_calib=n_calib)
+    lens_f = np.full(256, Lc)
+    pp = pages.plan(lens_f, w.sink, w.window, growth=0)
+    c = pages.allocate(pp, hkv=w.num_kv_heads, hq=w.num_q_heads, d=w.head_dim, sink=w.sink,
+                       window=w.window, device=dev, r_k=rot[0], r_v=rot[1], clip_k=rot[2],
+                       clip_v=rot[3])
+    lt = torch.tensor(lens_f.astype(np.int32), device=dev)
+
+    def pf():
+        L.oscar_prefill_quantize(c, di.k_tok, di.v_tok, di.seq_ids, di.positions, lt)
+    for _ in range(2):
+        pf()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    e0.record()
+    for _ in range(reps):
+        pf()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / reps
+    T = int(di.k_tok.shape[0])
+    i2b, bfb = token_bytes(w.head_dim)
+    n_i2 = 256 * max(0, Lc - w.window - w.sink)
+    rd = 2 * T * w.num_kv_heads * w.head_dim * 2
+    wr = w.num_kv_heads * (n_i2 * i2b + (T - n_i2) * bfb)
+    flops = 2 * 2 * n_i2 * w.num_kv_heads * w.head_dim * w.head_dim
+    res["prefill_256x4096"] = {"ms": round(t, 3), "tokens": T, "read_bytes": rd, "write_bytes": wr,
+                               "GBps": round((rd + wr) / t / 1e6, 1),
+                               "rotation_TFLOPs": round(flops / t / 1e9, 2)}
+    del c, di
     torch.cuda.empty_cache()
     return res
 
@@ -520,7 +664,7 @@ def main():
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     if args.profile:
         # launches in order: 1 prefill, then per step append, qrot, split, combine
-        dec = Decoder(inst, inst.seq_lens, rot, dev, l2_bytes=0)
+        dec = Decoder(device_inputs(inst, dev), rot, dev, l2_bytes=0)
         for i in range(args.warmup + args.steps):
             dec.step(i)
         torch.cuda.synchronize()
@@ -528,7 +672,8 @@ def main():
                           "launches_per_step": dec.launches_per_step,
                           "attention_bytes": int(dec.attn_bytes)}), flush=True)
         return
-    dec = Decoder(inst, inst.seq_lens, rot, dev, l2_bytes=l2)
+    di = device_inputs(inst, dev)
+    dec = Decoder(di, rot, dev, l2_bytes=l2)
     clocks = Clocks(local)
     ms, clk = time_steps(dec, args.steps, args.warmup, clocks=clocks, barrier=barrier)
     ms_all = ms
@@ -556,7 +701,7 @@ def main():
     # same-design BF16 kernel, same batch
     bf = {}
     try:
-        decb = Decoder(inst, inst.seq_lens, rot, dev, bf16_only=True, l2_bytes=l2)
+        decb = Decoder(di, rot, dev, bf16_only=True, l2_bytes=l2)
         msb, _ = time_steps(decb, min(args.steps, 1000), args.warmup)
         medb, meanb = time_decode_calls(decb, 100)
         bf = {"bf16_ms_per_step": round(msb, 5), "bf16_GBps": round(decb.step_bytes / msb / 1e6, 1),
@@ -601,11 +746,16 @@ def main():
     out.update(bf)
     if args.extras and rank == 0:
         ex = {}
-        for name in (synth.QWEN3_32B_128K.name,):
+        del dec
+        torch.cuda.empty_cache()
+        legs = ((synth.QWEN3_32B_128K.name, extra_long), (synth.QWEN3_4B_PREFIX.name, extra_prefix),
+                (synth.QWEN3_8B_BUDGET.name, extra_budget))
+        for name, fn in legs:
             try:
-                ex[name] = extra_decode(name, dev, l2, 2048)
+                ex[name] = fn(dev, l2, 2048)
             except Exception as e:
-                ex[name] = {"error": str(e)[:200]}
+                ex[name] = {"error": f"{type(e).__name__}: {str(e)[:300]}"}
+            torch.cuda.empty_cache()
         out["extras"] = ex
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inst, rot)

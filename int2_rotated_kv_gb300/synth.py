@@ -262,3 +262,101 @@ def ceil_div(a: int, b: int) -> int:
 
 def budget_batch(bytes_per_seq: int, budget: float) -> int:
     return int(math.floor(budget / bytes_per_seq))
+
+
+# ----------------------------------------------------------------------------
+# Large workloads, drawn on the GPU
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class DeviceInstance:
+    """A workload whose context is drawn on the GPU (torch), for sizes the host
+    generator would take minutes on.  Per-head parameters and calibration sets
+    come from the same seeded host streams as ``draw_instance``; context and
+    queries follow the same per-channel recipe from a seeded torch stream, so
+    values differ from ``draw_instance`` but the distribution does not.
+
+    Prefill lists hold tokens [0, L_b - 1) of every sequence (token-major
+    k/v [T, Hkv, d] bf16, seq_ids, positions); tokens of a shared prefix are
+    listed once, under sequence 0.  k_new/v_new are token L_b - 1 and q the
+    decode query at that position."""
+    workload: Workload
+    params: list
+    calib_q: list
+    calib_k: list
+    calib_v: list
+    seq_lens: np.ndarray
+    k_tok: object
+    v_tok: object
+    seq_ids: object
+    positions: object
+    k_new: object
+    v_new: object
+    q: object
+
+
+def _device_kv(gen, p: HeadParams, w: Workload, n: int, device):
+    import torch
+    d = w.head_dim
+    sk = torch.as_tensor(p.sigma_k, dtype=torch.float32, device=device)
+    sv = torch.as_tensor(p.sigma_v, dtype=torch.float32, device=device)
+    k = torch.randn((n, d), generator=gen, device=device) * sk
+    ko = torch.as_tensor(p.k_out, device=device)
+    k[:, ko] = k[:, ko] * w.k_outlier_mult + w.k_offset
+    v = torch.randn((n, d), generator=gen, device=device) * sv
+    vo = torch.as_tensor(p.v_out, device=device)
+    v[:, vo] = v[:, vo] * w.v_outlier_mult
+    return k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def draw_device(w: Workload, seq_lens, device, *, n_calib: int | None = None,
+                seed: int = 0) -> DeviceInstance:
+    import torch
+    root = np.random.default_rng(w.seed)
+    s_params, s_calib, _, _ = root.spawn(4)
+    H, G, d = w.num_kv_heads, w.gqa, w.head_dim
+    params = [head_params(r, w) for r in s_params.spawn(H)]
+    n_cal = w.n_calib if n_calib is None else n_calib
+    cq, ck, cv = [], [], []
+    for h, r in enumerate(s_calib.spawn(H)):
+        kk, vv = draw_kv(r, params[h], w, n_cal)
+        cq.append(draw_q(r, params[h], w, n_cal))
+        ck.append(kk)
+        cv.append(vv)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    B = len(lens)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1_000_003 * (w.seed + 1) + seed)
+    P = w.shared_prefix
+    prefix = [_device_kv(gen, params[h], w, P, device) for h in range(H)] if P else None
+    ks, vs, sids, poss = [], [], [], []
+    for b in range(B):
+        n = int(lens[b]) - 1                      # tokens already in the cache
+        first = P if (P and b > 0) else 0         # shared prefix listed under sequence 0 only
+        own = max(n - P, 0) if P else n
+        kb = torch.empty((n - first, H, d), dtype=torch.bfloat16, device=device)
+        vb = torch.empty_like(kb)
+        for h in range(H):
+            k_own, v_own = _device_kv(gen, params[h], w, own, device)
+            if P and b == 0:
+                kb[:, h] = torch.cat([prefix[h][0], k_own])[:n]
+                vb[:, h] = torch.cat([prefix[h][1], v_own])[:n]
+            else:
+                kb[:, h] = k_own[: n - first]
+                vb[:, h] = v_own[: n - first]
+        ks.append(kb)
+        vs.append(vb)
+        sids.append(torch.full((n - first,), b, dtype=torch.int32, device=device))
+        poss.append(torch.arange(first, n, dtype=torch.int32, device=device))
+    k_new = torch.empty((B, H, d), dtype=torch.bfloat16, device=device)
+    v_new = torch.empty_like(k_new)
+    q = torch.empty((B, H * G, d), dtype=torch.bfloat16, device=device)
+    for h in range(H):
+        a, c = _device_kv(gen, params[h], w, B, device)
+        k_new[:, h], v_new[:, h] = a, c
+        z = torch.randn((B, G, d), generator=gen, device=device)
+        std = torch.as_tensor(params[h].q_std, dtype=torch.float32, device=device)
+        basis = torch.as_tensor(params[h].q_basis, dtype=torch.float32, device=device)
+        q[:, h * G:(h + 1) * G] = ((z * std) @ basis.T).to(torch.bfloat16)
+    return DeviceInstance(w, params, cq, ck, cv, lens, torch.cat(ks), torch.cat(vs),
+                          torch.cat(sids), torch.cat(poss), k_new, v_new, q)
