@@ -15,6 +15,8 @@
 // rint((y_c - z16)/s16) clamped to [0,3], each step rounded in fp32 exactly as
 // written, then the codes are packed byte by byte into the page format of
 // layout.cuh (every byte holds codes of one token, so slots never collide).
+// Bulk prefill takes the tensor-core kernel of rotate_tc.cuh instead whenever
+// its inputs suit TMA; this kernel keeps the append and the other cases.
 #include <algorithm>
 
 #include "common.cuh"
@@ -62,6 +64,12 @@ struct QuantSmem {
 __device__ __forceinline__ void flag(int32_t* status, int bit) {
   if (status) atomicOr(status, bit);
 }
+
+}  // namespace oscar
+
+#include "rotate_tc.cuh"
+
+namespace oscar {
 
 template <int D>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p) {
@@ -378,7 +386,14 @@ oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k,
   p.seq_ids = seq_ids;
   p.positions = positions;
   p.seq_lens = seq_lens_final;
-  return oscar::dispatch(p, desc->head_dim, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the rotation on the tensor cores whenever the inputs suit TMA; the
+  // CUDA-core kernel otherwise (same bytes either way)
+  oscar_status r = OSCAR_OK;
+  const bool done = desc->head_dim == 128 ? oscar::launch_rotate_tc<128>(p, st, &r)
+                                          : oscar::launch_rotate_tc<64>(p, st, &r);
+  if (done) return r;
+  return oscar::dispatch(p, desc->head_dim, st);
 }
 
 oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_new,

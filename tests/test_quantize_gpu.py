@@ -43,7 +43,10 @@ def test_prefill_exact_rotation_is_bit_exact(kind, wl, lens):
 
 @pytest.mark.parametrize("wl,lens,W", [(synth.TINY, [512], 64),
                                        (synth.QWEN3_8B_32K, [1000, 2077, 131], 128),
-                                       (synth.QWEN3_32B_128K, [700], 128)])
+                                       (synth.QWEN3_32B_128K, [700], 128),
+                                       # ~86 tiles of 128 tokens: every CTA of the bulk
+                                       # prefill wraps its ring and both accumulators
+                                       (synth.QWEN3_8B_32K, [6000, 5000], 128)])
 def test_prefill_oscar_rotation_matches_oracle(wl, lens, W):
     inst = synth.draw_instance(wl, n_calib=512, seq_lens=lens)
     rot = H.oracle_rotations(inst)
