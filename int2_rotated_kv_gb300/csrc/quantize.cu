@@ -16,7 +16,8 @@
 // written, then the codes are packed byte by byte into the page format of
 // layout.cuh (every byte holds codes of one token, so slots never collide).
 // Bulk prefill takes the tensor-core kernel of rotate_tc.cuh instead whenever
-// its inputs suit TMA; this kernel keeps the append and the other cases.
+// its inputs suit TMA, and the per-step append has append_kernel (below); this
+// kernel keeps the prefill inputs that do not suit TMA.
 #include <algorithm>
 
 #include "common.cuh"
@@ -340,6 +341,152 @@ oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, quantize_kernel<D>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ append
+//
+// One decode step's append: per sequence b, the new token goes to its BF16 slot
+// (position L-1) and, once L-1-W >= S, the token at L-1-W leaves the window: it
+// is read back from its BF16 slot, rotated, clipped, quantised and packed into
+// its INT2 slot.  A batch has few tokens, so the work is spread over the
+// channel groups: a CTA owns one group of 32 output channels of one (KV head,
+// K/V) pair and up to 8 sequences, keeps the 16 KB column slice of R it needs,
+// and a warp handles one sequence (lane j = output channel 32*grp + j).
+constexpr int kAppendSeqs = 8;      // sequences per CTA: one per warp
+
+template <int D>
+__global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) {
+  constexpr int NG = D / 32;
+  __shared__ __align__(16) float rs[D][32];          // R[:, 32*grp .. 32*grp + 31]
+  __shared__ __align__(16) float xs[kQThreads / 32][D];
+  __shared__ uint8_t cs[kQThreads / 32][32];
+  const int grp = blockIdx.x % NG, chunk = blockIdx.x / NG;
+  const int h = blockIdx.y, kv = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // programmatic stream serialisation: inputs are read only after the
+  // predecessor grid has completed; then the next kernel may launch
+  pdl_wait();
+  pdl_trigger();
+  const float* rot = (kv ? p.r_v : p.r_k) + static_cast<size_t>(h) * D * D + 32 * grp;
+  for (int e = tid; e < D * 8; e += kQThreads) {       // float4 e%8 of row e/8
+    const int i = e >> 3, c4 = e & 7;
+    reinterpret_cast<float4*>(&rs[i][0])[c4] = reinterpret_cast<const float4*>(rot + i * D)[c4];
+  }
+  __syncthreads();
+  const float clip = (kv ? p.clip_v : p.clip_k)[h];
+  const uint16_t* src = kv ? p.v_src : p.k_src;
+  const int j = 32 * grp + lane;                       // this lane's channel
+  for (int u = warp; u < kAppendSeqs; u += kQThreads / 32) {
+    const int b = chunk * kAppendSeqs + u;
+    if (b >= p.n_items) break;
+    const int L = p.seq_lens[b];
+    if (L < 1 || (L - 1) / kPage >= p.max_pages) {
+      if (lane == 0 && grp == 0) flag(p.status, OSCAR_DEVERR_SEQ_LEN);
+      continue;
+    }
+    const int64_t base = static_cast<int64_t>(b) * p.max_pages;
+    // the new token's channel j -> its BF16 slot
+    const int pn = L - 1;
+    const int pg = p.bf16_pt[base + pn / kPage];
+    if (pg < 0 || pg >= p.n_bf16_pages) {
+      if (lane == 0 && grp == 0) flag(p.status, OSCAR_DEVERR_PAGE_ID);
+    } else {
+      const int e = kv ? 16 * D + bf16_value_elem(pn % kPage, j) : bf16_key_elem(pn % kPage, j);
+      p.bf16_pool[(static_cast<int64_t>(pg) * p.hkv + h) * (32 * D) + e] =
+          src[(static_cast<int64_t>(b) * p.hkv + h) * D + j];
+    }
+    // the token leaving the window
+    const int po = L - 1 - p.window;
+    if (po < p.sink) continue;
+    const int sp = p.bf16_pt[base + po / kPage];
+    const int dp = p.int2_pt[base + po / kPage];
+    if (sp < 0 || sp >= p.n_bf16_pages || dp < 0 || dp >= p.n_int2_pages) {
+      if (lane == 0 && grp == 0) flag(p.status, OSCAR_DEVERR_PAGE_ID);
+      continue;
+    }
+    const int slot = po % kPage;
+    const uint16_t* sblk = p.bf16_pool + (static_cast<int64_t>(sp) * p.hkv + h) * (32 * D);
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      const int jj = 32 * c + lane;
+      const int e = kv ? 16 * D + bf16_value_elem(slot, jj) : bf16_key_elem(slot, jj);
+      xs[warp][jj] = bf16_to_float(sblk[e]);
+    }
+    __syncwarp();
+    // y_j = sum_i x_i R[i][j], fp32, four partial chains over i
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int i = 0; i < D; i += 4) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[warp][i]);
+      acc[0] = fmaf(xv.x, rs[i][lane], acc[0]);
+      acc[1] = fmaf(xv.y, rs[i + 1][lane], acc[1]);
+      acc[2] = fmaf(xv.z, rs[i + 2][lane], acc[2]);
+      acc[3] = fmaf(xv.w, rs[i + 3][lane], acc[3]);
+    }
+    const float y = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    const float yc = fminf(fmaxf(y, -clip), clip);
+    const float mn = warp_min(yc);
+    const float mx = warp_max(yc);
+    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+    const __half z16 = __float2half_rn(mn);
+    const float sf = __half2float(s16);
+    const float zf = __half2float(z16);
+    int code = 0;
+    if (sf != 0.f) code = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(yc, zf), sf)), 0), 3);
+    cs[warp][lane] = static_cast<uint8_t>(code);
+    __syncwarp();
+    uint8_t* blk = p.int2_pool + (static_cast<int64_t>(dp) * p.hkv + h) * Fmt<D>::kInt2Block;
+    const uint8_t* ct = cs[warp];
+    if (lane < 8) {   // 8 code bytes of this group
+      uint32_t byte = 0;
+      if (kv == 0) {
+        const int tig = lane >> 1, e = lane & 1;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            byte |= static_cast<uint32_t>(ct[16 * i + 8 * hh + 2 * tig + e]) << (4 * hh + 2 * i);
+        blk[Fmt<D>::kKc + key_byte<D>(slot, tig, grp, e)] = static_cast<uint8_t>(byte);
+      } else {
+        const int gid = lane;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            byte |= static_cast<uint32_t>(ct[16 * i + 8 * ch + gid]) << (4 * ch + 2 * i);
+        blk[Fmt<D>::kVc + value_byte<D>(slot, gid, grp)] = static_cast<uint8_t>(byte);
+      }
+    } else if (lane == 8) {
+      const uint32_t sz = static_cast<uint32_t>(__half_as_ushort(s16)) |
+                          (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+      if (kv == 0) {
+        reinterpret_cast<uint32_t*>(blk + Fmt<D>::kKsz)[slot * NG + grp] = sz;
+      } else {
+        const int e = vsz_index<D>(slot, grp);
+        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
+        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVz)[e] = static_cast<uint16_t>(sz >> 16);
+      }
+    }
+    __syncwarp();
+  }
+}
+
+template <int D>
+oscar_status launch_append(const QuantParams& p, cudaStream_t st) {
+  const int64_t chunks = (p.n_items + kAppendSeqs - 1) / kAppendSeqs;
+  if (chunks == 0) return OSCAR_OK;
+  const dim3 grid(static_cast<unsigned>(chunks * (D / 32)), p.hkv, 2);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, append_kernel<D>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
 QuantParams base_params(const oscar_cache_desc* c) {
   QuantParams p{};
   p.hkv = c->num_kv_heads;
@@ -411,7 +558,8 @@ oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_n
   p.k_src = static_cast<const uint16_t*>(k_new);
   p.v_src = static_cast<const uint16_t*>(v_new);
   p.seq_lens = seq_lens_after;
-  return oscar::dispatch(p, desc->head_dim, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return desc->head_dim == 128 ? oscar::launch_append<128>(p, st) : oscar::launch_append<64>(p, st);
 }
 
 }  // extern "C"
