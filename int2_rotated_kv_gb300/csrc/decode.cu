@@ -352,8 +352,12 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
   const size_t pstride = static_cast<size_t>(p.hkv) * SB;
   const int my_n = n > warp ? (n - warp + kDWarps - 1) / kDWarps : 0;
   const int* wids = ids + warp;                   // page i of this warp: wids[8 i]
+  // Only kPreStages pages per warp are requested before the rotated query is
+  // read: a full ring from every CTA at once queues the small q' loads behind
+  // megabytes of page copies.  The rest of the ring follows the staging.
+  constexpr int kPreStages = 2;
   if (lane == 0) {
-    for (int i = 0; i < min(NS, my_n); ++i) {
+    for (int i = 0; i < min(kPreStages, my_n); ++i) {
       mbar_arrive_expect_tx(&wbar[i], SB);
       bulk_g2s(wring + i * SB, pool_h + max(wids[kDWarps * i], 0) * pstride, SB, &wbar[i]);
     }
@@ -397,6 +401,12 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     }
   }
   __syncthreads();
+  if (lane == 0) {
+    for (int i = kPreStages; i < min(NS, my_n); ++i) {
+      mbar_arrive_expect_tx(&wbar[i], SB);
+      bulk_g2s(wring + i * SB, pool_h + max(wids[kDWarps * i], 0) * pstride, SB, &wbar[i]);
+    }
+  }
   const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
   const int tok_lo = p.sink, tok_hi = L - p.window;
   uint32_t phase = 0;
