@@ -261,7 +261,7 @@ class Decoder:
         ws = L.oscar_decode_workspace_size(base, B, self.max_len)
         self.ws = torch.empty(ws // 4 + 64, dtype=torch.float32, device=dev)
         self.n_layers = n_layers
-        self.launches_per_step = 4 if not bf16_only else 3
+        self.launches_per_step = 3     # INT2: append+q', split, combine; BF16: append, split, combine
 
     def append(self, i, k=None, v=None, lens=None):
         c = self.caches[i % self.n_layers]
@@ -274,9 +274,15 @@ class Decoder:
         fn(c, self.q if q is None else q, self.lens_dev if lens is None else lens, self.max_len,
            self.out if out is None else out, self.ws)
 
-    def step(self, i):
-        self.append(i)
-        self.attend(i)
+    def step(self, i, q=None, k=None, v=None, out=None):
+        if self.bf16_only:
+            self.append(i, k, v)
+            self.attend(i, q, out=out)
+        else:   # the library's fused step: append + attention in one call
+            c = self.caches[i % self.n_layers]
+            self.L.oscar_decode_step(c, self.q if q is None else q, self.k_new if k is None else k,
+                                     self.v_new if v is None else v, self.lens_dev, self.max_len,
+                                     self.out if out is None else out, self.ws)
 
     def graph(self, first, count):
         torch = self.torch
@@ -394,8 +400,7 @@ def time_e2e(dec, steps, warmup):
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        dec.append(i, dk, dv)
-        dec.attend(i, dq, out=do)
+        dec.step(i, dq, dk, dv, do)
         ho.copy_(do, non_blocking=True)
 
     for i in range(warmup):
@@ -663,7 +668,7 @@ def main():
     t_cal = time.time() - t0
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     if args.profile:
-        # launches in order: 1 prefill, then per step append, qrot, split, combine
+        # launches in order: 1 prefill, then per step the fused append (+ q'), split, combine
         dec = Decoder(device_inputs(inst, dev), rot, dev, l2_bytes=0)
         for i in range(args.warmup + args.steps):
             dec.step(i)
@@ -726,7 +731,7 @@ def main():
                    "n_calib": n_calib, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: steps rotate over {dec.n_layers} layer caches "
                          f"({dec.n_layers * dec.attn_bytes / 1e6:.0f} MB touched vs L2 {l2 / 1e6:.0f} MB)",
-                   "step": "oscar_quantize_append + oscar_decode_attention, one layer, CUDA graph"},
+                   "step": "oscar_decode_step (append + attention fused), one layer, CUDA graph"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "oscar_decode_attention call (qrot + split + combine kernels)",

@@ -181,6 +181,22 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
                                          int32_t max_seq_len, void* out, void* workspace,
                                          size_t workspace_bytes, void* stream);
 
+/* One decode step over the mixed cache: oscar_quantize_append (the new token
+ * into its BF16 slot, the token leaving the recent window rotated, clipped,
+ * quantised and packed into its INT2 slot) followed by oscar_decode_attention
+ * at the new lengths, as one fused pipeline ("Technical Summary: OSCAR ...",
+ * section 2.2B: compatibility with fused kernel pipelines).  The append kernel
+ * also computes the step's rotated query q' = q R_K, so no separate rotation
+ * kernel runs; the attention kernels copy the pages the append writes only
+ * after it has completed.  Arguments: q, out as oscar_decode_attention;
+ * k_new, v_new, seq_lens_after as oscar_quantize_append (seq_lens_after is the
+ * length including the new token); workspace as oscar_decode_attention (the
+ * same size).  Result equals the two calls in sequence. */
+oscar_status oscar_decode_step(const oscar_cache_desc* desc, const void* q, const void* k_new,
+                               const void* v_new, const int32_t* seq_lens_after, int32_t batch,
+                               int32_t max_seq_len, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* oscar_decode_attention for callers that cannot allocate device memory.
  * The pages describe no counterpart; it exists because some callers have no
  * allocator at hand when they run attention: a plug-in inside a runtime that

@@ -24,7 +24,8 @@ VARIANT_OSCAR, VARIANT_HADAMARD, VARIANT_IDENTITY = 0, 1, 2
 EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rotation",
             "oscar_prefill_quantize", "oscar_quantize_append", "oscar_decode_workspace_size",
             "oscar_decode_attention", "oscar_decode_attention_bf16", "oscar_device_sm_count",
-            "oscar_status_string", "oscar_version", "oscar_decode_attention_static")
+            "oscar_status_string", "oscar_version", "oscar_decode_attention_static",
+            "oscar_decode_step")
 
 
 class OscarError(RuntimeError):
@@ -70,6 +71,7 @@ def lib() -> ctypes.CDLL:
             "oscar_decode_attention_bf16": (I32, [P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_device_sm_count": (I32, []),
             "oscar_decode_attention_static": (I32, [P, P, P, I32, I32, P, P]),
+            "oscar_decode_step": (I32, [P, P, P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_status_string": (ctypes.c_char_p, [I32]),
             "oscar_version": (I32, []),
         }
@@ -225,6 +227,19 @@ def oscar_decode_attention_bf16(cache: Cache, q, seq_lens, max_seq_len: int, out
                                              _ptr(workspace),
                                              workspace.numel() * workspace.element_size(),
                                              _stream(stream)))
+
+
+def oscar_decode_step(cache: Cache, q, k_new, v_new, seq_lens_after, max_seq_len: int, out,
+                      workspace, stream=None):
+    """Append the step's new token (and move the one leaving the window to INT2),
+    then attend at the new lengths: one fused call, same result as
+    oscar_quantize_append followed by oscar_decode_attention."""
+    d = cache.desc()
+    _check("oscar_decode_step",
+           lib().oscar_decode_step(ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                   _ptr(seq_lens_after), int(seq_lens_after.numel()),
+                                   int(max_seq_len), _ptr(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def oscar_decode_attention_static(cache: Cache, q, seq_lens, max_seq_len: int, out, stream=None):

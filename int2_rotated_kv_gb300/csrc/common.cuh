@@ -2,6 +2,7 @@
 // transpose, mbarriers, bulk (TMA) copies and programmatic dependent launch.
 #pragma once
 
+#include <cuda.h>           // CUtensorMap and its enums; the encoder is fetched at run time
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -170,6 +171,27 @@ __device__ __forceinline__ float warp_min(float v) {
 // ------------------------------------------------------------ host helpers
 
 namespace oscar_host {
+
+typedef CUresult (*TensorMapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                         const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                         const cuuint32_t*, CUtensorMapInterleave,
+                                         CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                         CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time
+// dependency on the driver library); null when unavailable.
+inline TensorMapEncodeTiled tensor_map_encoder() {
+  static TensorMapEncodeTiled fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<TensorMapEncodeTiled>(nullptr);
+    return reinterpret_cast<TensorMapEncodeTiled>(f);
+  }();
+  return fn;
+}
 
 inline bool head_dim_ok(int d) { return d == 64 || d == 128; }
 

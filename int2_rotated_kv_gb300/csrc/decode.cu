@@ -67,6 +67,10 @@ struct DecodeParams {
   float* part;    // [B][Hq][n_splits][D + 2]
   float scale_log2;
   int wait_first; // wait for the predecessor grid before reading any input
+  // launched right after the step's append kernel (no rotation kernel between):
+  // pages that kernel writes -- the INT2 page of the token leaving the window,
+  // the BF16 page of the new token -- are copied only after griddepcontrol.wait
+  int after_append;
 };
 
 // ------------------------------------------------------------------ q R_K
@@ -341,7 +345,7 @@ template <int D, int NS>
 __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, int lo, int n, int L, uint8_t* ring,
                                            uint64_t* bars, uint2* qbs, float (&o)[D / 16][4],
-                                           float (&zacc)[4], Softmax& sm) {
+                                           float (&zacc)[4], Softmax& sm, int defer_lp) {
   static_assert(NS % 2 == 0, "pages are consumed in pairs of stages");
   constexpr int NG = D / 32, NK = D / 16;
   constexpr int SB = Fmt<D>::kInt2Block;
@@ -355,9 +359,16 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
   // Only kPreStages pages per warp are requested before the rotated query is
   // read: a full ring from every CTA at once queues the small q' loads behind
   // megabytes of page copies.  The rest of the ring follows the staging.
+  // A page the predecessor grid may still be writing (defer_lp) waits for the
+  // second batch.
   constexpr int kPreStages = 2;
+  int deferred = -1;
   if (lane == 0) {
     for (int i = 0; i < min(kPreStages, my_n); ++i) {
+      if (lo + warp + kDWarps * i == defer_lp) {
+        deferred = i;
+        continue;
+      }
       mbar_arrive_expect_tx(&wbar[i], SB);
       bulk_g2s(wring + i * SB, pool_h + max(wids[kDWarps * i], 0) * pstride, SB, &wbar[i]);
     }
@@ -402,6 +413,11 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
   }
   __syncthreads();
   if (lane == 0) {
+    if (deferred >= 0) {
+      mbar_arrive_expect_tx(&wbar[deferred], SB);
+      bulk_g2s(wring + deferred * SB, pool_h + max(wids[kDWarps * deferred], 0) * pstride, SB,
+               &wbar[deferred]);
+    }
     for (int i = kPreStages; i < min(NS, my_n); ++i) {
       mbar_arrive_expect_tx(&wbar[i], SB);
       bulk_g2s(wring + i * SB, pool_h + max(wids[kDWarps * i], 0) * pstride, SB, &wbar[i]);
@@ -479,16 +495,20 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
   const uint8_t* pool_h = p.bf16_pool + static_cast<size_t>(h) * SB;
   const size_t pstride = static_cast<size_t>(p.hkv) * SB;
   const int my_n = n > warp ? (n - warp + kDWarps - 1) / kDWarps : 0;
-  if (lane == 0) {
-    for (int i = 0; i < min(NS, my_n); ++i) {
-      const int id = ids[warp + kDWarps * i];
-      if (id >= 0) {
-        mbar_arrive_expect_tx(&wbar[i], SB);
-        bulk_g2s(wring + i * SB, pool_h + id * pstride, SB, &wbar[i]);
+  auto prefill = [&] {
+    if (lane == 0) {
+      for (int i = 0; i < min(NS, my_n); ++i) {
+        const int id = ids[warp + kDWarps * i];
+        if (id >= 0) {
+          mbar_arrive_expect_tx(&wbar[i], SB);
+          bulk_g2s(wring + i * SB, pool_h + id * pstride, SB, &wbar[i]);
+        }
       }
     }
-  }
+  };
+  if (!p.after_append) prefill();   // the new token's BF16 page may still be in writing
   pdl_wait();
+  if (p.after_append) prefill();
   uint32_t qb[NK][2];
   {
     const uint16_t* qr = p.q + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
@@ -633,9 +653,11 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   for (int t = 0; t < NK; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
   float zacc[4] = {0.f, 0.f, 0.f, 0.f};
   Softmax sm{-INFINITY, -INFINITY, 0.f, 0.f};
+  // the INT2 page receiving the token that leaves the window in this step
+  const int defer_lp = (p.after_append && L - 1 - p.window >= p.sink) ? (L - 1 - p.window) / kPage : -1;
   if (mode == 0)
     int2_pages<D, C::kStagesI>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
-                               reinterpret_cast<uint2*>(lps), o, zacc, sm);
+                               reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp);
   else
     bf16_pages<D, C::kStagesB>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm);
 
@@ -900,8 +922,10 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
   // start while its predecessor drains, and waits (griddepcontrol.wait) before
   // touching anything the predecessor produces
   if (!kBf16Only) {
-    e = launch_pdl(qrot_kernel<D>, dim3(p.hkv, p.batch), dim3(1024), 0, st, p);
-    if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+    if (!p.after_append) {   // a fused step's append kernel has written q' already
+      e = launch_pdl(qrot_kernel<D>, dim3(p.hkv, p.batch), dim3(1024), 0, st, p);
+      if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+    }
     e = launch_pdl(split_kernel<D, kBf16Only>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   } else {
     e = launch_pdl(split_kernel<D, kBf16Only>, sgrid, dim3(kDThreads), C::kBytes, st, p);
@@ -911,9 +935,14 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
+oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, const void* k_new,
+                               const void* v_new, const int32_t* seq_lens_after, int32_t batch,
+                               float* qrot, cudaStream_t st);
+
 oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_t* seq_lens,
                           int batch, int max_len, void* out, void* ws, size_t ws_bytes,
-                          void* stream, bool bf16_only) {
+                          void* stream, bool bf16_only, const void* k_new = nullptr,
+                          const void* v_new = nullptr) {
   oscar_status s = oscar_host::check_desc(c, !bf16_only, true);
   if (s != OSCAR_OK) return s;
   if (batch < 0 || max_len < 1) return OSCAR_ERR_INVALID_ARG;
@@ -958,6 +987,11 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->head_dim)));
   p.wait_first = bf16_only ? 1 : 0;   // the INT2 call is gated by qrot_kernel
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (k_new) {   // fused step: the append kernel writes q' and gates the split kernel
+    p.after_append = 1;
+    const oscar_status a = append_with_query(c, q, k_new, v_new, seq_lens, batch, p.qrot, st);
+    if (a != OSCAR_OK) return a;
+  }
   if (c->head_dim == 128)
     return bf16_only ? run_decode<128, true>(p, pl, st) : run_decode<128, false>(p, pl, st);
   return bf16_only ? run_decode<64, true>(p, pl, st) : run_decode<64, false>(p, pl, st);
@@ -1055,6 +1089,15 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
 }
 
 int32_t oscar_device_sm_count(void) { return oscar_host::sm_count(); }
+
+oscar_status oscar_decode_step(const oscar_cache_desc* desc, const void* q, const void* k_new,
+                               const void* v_new, const int32_t* seq_lens_after, int32_t batch,
+                               int32_t max_seq_len, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (batch > 0 && (!k_new || !v_new)) return OSCAR_ERR_INVALID_ARG;
+  return oscar::decode_entry(desc, q, seq_lens_after, batch, max_seq_len, out, workspace,
+                             workspace_bytes, stream, false, batch > 0 ? k_new : nullptr, v_new);
+}
 
 oscar_status oscar_decode_attention_static(const oscar_cache_desc* desc, const void* q,
                                            const int32_t* seq_lens, int32_t batch,

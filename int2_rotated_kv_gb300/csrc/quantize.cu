@@ -48,6 +48,11 @@ struct QuantParams {
   const int32_t* seq_ids;
   const int32_t* positions;
   const int32_t* seq_lens;
+  // append only, optional: the step's rotated query q' = q R_K, written by the
+  // K-side CTAs (each its 32 output channels) for the decode that follows
+  const uint16_t* q;     // [B][Hq][D] bf16
+  float* qrot;           // [B][Hq][D] fp32, or null
+  int hq, G;
 };
 
 template <int D>
@@ -374,6 +379,31 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
   const float clip = (kv ? p.clip_v : p.clip_k)[h];
   const uint16_t* src = kv ? p.v_src : p.k_src;
   const int j = 32 * grp + lane;                       // this lane's channel
+  if (kv == 0 && p.qrot) {
+    // the step's rotated query: one (sequence, query head) task per warp, lane j
+    // computing channel 32*grp + j
+    const int64_t left = p.n_items - static_cast<int64_t>(chunk) * kAppendSeqs;
+    const int n_seq = static_cast<int>(left < kAppendSeqs ? left : kAppendSeqs);
+    for (int task = warp; task < n_seq * p.G; task += kQThreads / 32) {
+      const int b = chunk * kAppendSeqs + task / p.G, g = task % p.G;
+      const uint16_t* qg = p.q + (static_cast<int64_t>(b) * p.hq + h * p.G + g) * D;
+#pragma unroll
+      for (int c = 0; c < NG; ++c) xs[warp][32 * c + lane] = bf16_to_float(qg[32 * c + lane]);
+      __syncwarp();
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int i = 0; i < D; i += 4) {
+        const float4 xv = *reinterpret_cast<const float4*>(&xs[warp][i]);
+        acc[0] = fmaf(xv.x, rs[i][lane], acc[0]);
+        acc[1] = fmaf(xv.y, rs[i + 1][lane], acc[1]);
+        acc[2] = fmaf(xv.z, rs[i + 2][lane], acc[2]);
+        acc[3] = fmaf(xv.w, rs[i + 3][lane], acc[3]);
+      }
+      p.qrot[(static_cast<int64_t>(b) * p.hq + h * p.G + g) * D + j] =
+          (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      __syncwarp();
+    }
+  }
   for (int u = warp; u < kAppendSeqs; u += kQThreads / 32) {
     const int b = chunk * kAppendSeqs + u;
     if (b >= p.n_items) break;
@@ -509,6 +539,25 @@ QuantParams base_params(const oscar_cache_desc* c) {
 
 oscar_status dispatch(const QuantParams& p, int d, cudaStream_t st) {
   return d == 128 ? launch_quantize<128>(p, st) : launch_quantize<64>(p, st);
+}
+
+// The append of a fused decode step: as oscar_quantize_append, and the K-side
+// CTAs also write q' = q R_K for the decode that follows.
+oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, const void* k_new,
+                               const void* v_new, const int32_t* seq_lens_after, int32_t batch,
+                               float* qrot, cudaStream_t st) {
+  QuantParams p = base_params(desc);
+  p.append = 1;
+  p.n_items = batch;
+  p.num_seqs = batch;
+  p.k_src = static_cast<const uint16_t*>(k_new);
+  p.v_src = static_cast<const uint16_t*>(v_new);
+  p.seq_lens = seq_lens_after;
+  p.q = static_cast<const uint16_t*>(q);
+  p.qrot = qrot;
+  p.hq = desc->num_q_heads;
+  p.G = desc->num_q_heads / desc->num_kv_heads;
+  return desc->head_dim == 128 ? launch_append<128>(p, st) : launch_append<64>(p, st);
 }
 
 }  // namespace oscar

@@ -34,7 +34,6 @@
 // its copies and MMAs in flight before it frees tensor memory.
 #pragma once
 
-#include <cuda.h>          // CUtensorMap and its enums; the encoder is fetched at run time
 #include <cuda_bf16.h>
 
 namespace oscar {
@@ -468,29 +467,10 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
 
 // ------------------------------------------------------------------- host
 
-typedef CUresult (*TensorMapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                         const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                         const cuuint32_t*, CUtensorMapInterleave,
-                                         CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                         CUtensorMapFloatOOBfill);
-
-inline TensorMapEncodeTiled tensor_map_encoder() {
-  static TensorMapEncodeTiled fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<TensorMapEncodeTiled>(nullptr);
-    return reinterpret_cast<TensorMapEncodeTiled>(f);
-  }();
-  return fn;
-}
-
 // 2-D view [rows = tokens][cols = Hkv * d] of a bf16 token-major K or V array;
 // boxes of 64 channels x 128 tokens, 128-byte swizzled, zero fill past the end.
 inline bool make_token_map(CUtensorMap* m, const void* base, int64_t rows, int cols) {
-  TensorMapEncodeTiled enc = tensor_map_encoder();
+  oscar_host::TensorMapEncodeTiled enc = oscar_host::tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};

@@ -3,7 +3,7 @@ through its C ABI, read pools back.  Expected values come from ``oracle`` only."
 import numpy as np
 
 from int2_rotated_kv_gb300 import pages, synth
-from oracle import attention, cache as ocache, layout
+from oracle import attention, cache as ocache, layout, quant
 
 DEV = "cuda:0"
 TOL_MAX_ABS = 1e-2       # attention output vs oracle (fp32 accumulate, bf16 store)
@@ -74,7 +74,8 @@ def prefill(cache, inst, lens=None, upto=None):
 
 def pools(cache):
     t = torch()
-    t.cuda.synchronize()
+    if t.cuda.is_available():
+        t.cuda.synchronize()
     return cache.int2_pool.cpu().numpy(), cache.bf16_pool.view(t.int16).cpu().numpy().view(np.uint16)
 
 
@@ -114,6 +115,48 @@ def decode(cache, q, lens, max_len=None, bf16_only=False, out=None):
     fn(cache, qt, lt, max_len, o, ws)
     t.cuda.synchronize()
     return from_bf16(o)
+
+
+def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa):
+    """The oracle's attention over what the GPU actually stored: every token of
+    every sequence read back from the pools (INT2 codes, s16, z16 dequantised and
+    rotated back with R^T; BF16 tokens as stored), then fp64 softmax attention.
+    Separates the decode kernels' parity from the quantiser's (whose flagged
+    near-boundary codes may differ from the oracle's by one step)."""
+    got2, gotb = pools(cache)
+    B, Hq, d = q.shape
+    hkv = Hq // gqa
+    blk2 = layout.int2_block_bytes(d)
+    blkb = layout.bf16_block_bytes(d) // 2
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        L = int(lens[b])
+        t = np.arange(L)
+        m = ocache.is_int2(t, L, sink, window)
+        for h in range(hkv):
+            k = np.zeros((L, d))
+            v = np.zeros((L, d))
+            for pg in range((L + 15) // 16):
+                ts = t[16 * pg:16 * pg + 16]
+                slots = ts - 16 * pg
+                mi = m[ts]
+                if mi.any():
+                    pid = int(pp.int2_table[b, pg])
+                    kc, ks, kz, vc, vs, vz = layout.unpack_int2_block(
+                        got2[(pid * hkv + h) * blk2:(pid * hkv + h + 1) * blk2], d)
+                    sl = slots[mi]
+                    yk = quant.dequantize(kc[sl], ks[sl], kz[sl])
+                    yv = quant.dequantize(vc[sl], vs[sl], vz[sl])
+                    k[ts[mi]] = yk @ np.asarray(rot.rk[h], np.float64).T
+                    v[ts[mi]] = yv @ np.asarray(rot.rv[h], np.float64).T
+                if (~mi).any():
+                    pid = int(pp.bf16_table[b, pg])
+                    kb, vb = layout.unpack_bf16_block(gotb[(pid * hkv + h) * blkb:(pid * hkv + h + 1) * blkb], d)
+                    sl = slots[~mi]
+                    k[ts[~mi]] = synth.bf16_from_bits(kb[sl])
+                    v[ts[~mi]] = synth.bf16_from_bits(vb[sl])
+            out[b, h * gqa:(h + 1) * gqa] = attention.softmax_attention(q[b, h * gqa:(h + 1) * gqa], k, v)
+    return out
 
 
 def status(cache):

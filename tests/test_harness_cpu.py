@@ -1,0 +1,28 @@
+"""Pins for test infrastructure that turns stored pools back into attention."""
+import types
+
+import numpy as np
+
+import gpu_harness as H
+from int2_rotated_kv_gb300 import pages, synth
+from oracle import attention, cache as ocache
+
+
+def test_attention_from_pools_reproduces_the_oracle():
+    """Pools packed by the oracle, read back and attended, give exactly the
+    oracle's mixed-cache attention (both are fp64 over the same stored values)."""
+    import torch
+    wl = synth.TINY
+    lens = np.array([300, 77, 66])
+    inst = synth.draw_instance(wl, n_calib=256, seq_lens=lens)
+    rot = attention.calibrate(inst.calib_q, inst.calib_k, inst.calib_v, 0)
+    pp = pages.plan(lens, 4, 64, permute_seed=5)
+    exp = ocache.expected_pools(inst.k, inst.v, lens, rot, sink=4, window=64, d=wl.head_dim,
+                                hkv=wl.num_kv_heads, int2_table=pp.int2_table,
+                                bf16_table=pp.bf16_table, num_int2_pages=pp.num_int2_pages,
+                                num_bf16_pages=pp.num_bf16_pages)
+    cache = types.SimpleNamespace(int2_pool=torch.from_numpy(exp.int2.copy()),
+                                  bf16_pool=torch.from_numpy(exp.bf16.view(np.int16).copy()).view(torch.bfloat16))
+    got = H.attention_from_pools(cache, pp, inst.q, lens, rot, sink=4, window=64, gqa=wl.gqa)
+    ref = attention.mixed_decode(inst.q, inst.k, inst.v, lens, rot, sink=4, window=64, gqa=wl.gqa)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
