@@ -62,6 +62,22 @@ def parse():
 
 # --------------------------------------------------------------------------- util
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: the job is done when every replica is."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(step_bytes_per_rank, ms_all, world):
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * step_bytes_per_rank / (ms_all * 1e-3) / 1e9
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -681,13 +697,8 @@ def main():
     dec = Decoder(di, rot, dev, l2_bytes=l2)
     clocks = Clocks(local)
     ms, clk = time_steps(dec, args.steps, args.warmup, clocks=clocks, barrier=barrier)
-    ms_all = ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_all = float(t.item())
-    value = world * dec.step_bytes / (ms_all * 1e-3) / 1e9
+    ms_all = max_over_ranks(ms, world, dev)
+    value = job_gbps(dec.step_bytes, ms_all, world)
     # roofline of the decode call (qrot + split + combine), cold L2
     med, mean = time_decode_calls(dec, 200)
     peak, peak_kind = peaks()
@@ -702,7 +713,7 @@ def main():
         pass
     # end to end through the C ABI with host buffers
     e2e_ms, h2d, d2h = time_e2e(dec, min(args.steps, 500), max(3, args.warmup))
-    e2e_val = world * dec.step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_val = job_gbps(dec.step_bytes, max_over_ranks(e2e_ms, world, dev), world)
     # same-design BF16 kernel, same batch
     bf = {}
     try:
