@@ -480,6 +480,38 @@ def cpu_baseline(inst, rot, budget_s=12.0, max_passes=400):
                       f"context of sequence 0); {tot_t:.1f} s of CPU work"}
 
 
+def cpu_one_thread_sample(workload_name, budget_s=6.0):
+    """The oracle's decode pass timed in a child process whose BLAS / OpenMP pools
+    are limited to one thread (they are fixed when numpy loads, so a fresh
+    process is needed).  No GPU is touched there."""
+    code = (
+        "import json, sys, time, numpy as np\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import bench\n"
+        "from int2_rotated_kv_gb300 import synth\n"
+        "from oracle import attention\n"
+        f"w = synth.WORKLOADS[{workload_name!r}]\n"
+        "inst = synth.draw_instance(w, n_calib=512)\n"
+        "r = attention.calibrate(inst.calib_q, inst.calib_k, inst.calib_v, 0)\n"
+        "rot = (np.stack(r.rk), np.stack(r.rv), np.array(r.ck), np.array(r.cv))\n"
+        "tb = tt = 0.0\n"
+        "heads = 0\n"
+        f"while tt < {budget_s} and heads < 64:\n"
+        "    b, t = bench.oracle_sample(inst, rot, 1)\n"
+        "    tb += b; tt += t; heads += 1\n"
+        "print(json.dumps({'value': tb / tt / 1e9, 'heads': heads, 'seconds': tt}))\n")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                           timeout=600)
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": round(res["value"], 4), "unit": UNIT, "cores": 1,
+                "sample": f"{res['heads']} single-KV-head pass(es), {res['seconds']:.1f} s"}
+    except Exception as e:
+        return {"error": str(e)[:200]}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -775,6 +807,7 @@ def main():
         out["extras"] = ex
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inst, rot)
+        out["cpu_baseline"]["one_thread"] = cpu_one_thread_sample(w.name)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

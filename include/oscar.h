@@ -25,7 +25,8 @@
  *
  * Cache format (one layer).  Page size 16 tokens, quantisation group 32
  * channels, head_dim d in {64, 128}, G = num_q_heads / num_kv_heads in
- * {1, 2, 4, 8}.  A sequence of length L (current token included) keeps tokens
+ * {1, 2, 4, 8, 16} (G = 16 is served as two halves of 8 query heads, each of
+ * which reads the KV head's pages).  A sequence of length L (current token included) keeps tokens
  * t < sink and t >= L - window in BF16 pages, and tokens sink <= t < L - window
  * in INT2 pages [Summary 2.2B, "Mixed-Precision Layout"].  Logical page
  * p = t / 16 of sequence b maps to a physical page through two tables of int32

@@ -204,7 +204,7 @@ inline oscar_status check_desc(const oscar_cache_desc* c, bool needs_int2, bool 
   if (!head_dim_ok(c->head_dim)) return OSCAR_ERR_UNSUPPORTED;
   if (c->num_q_heads % c->num_kv_heads) return OSCAR_ERR_INVALID_ARG;
   const int g = c->num_q_heads / c->num_kv_heads;
-  if (!(g == 1 || g == 2 || g == 4 || g == 8)) return OSCAR_ERR_UNSUPPORTED;
+  if (!(g == 1 || g == 2 || g == 4 || g == 8 || g == 16)) return OSCAR_ERR_UNSUPPORTED;
   if (needs_bf16 && (!c->bf16_pool || !c->bf16_page_table || c->num_bf16_pages < 1))
     return OSCAR_ERR_INVALID_ARG;
   if (needs_int2 && (!c->int2_pool || !c->int2_page_table || c->num_int2_pages < 1 || !c->r_k ||

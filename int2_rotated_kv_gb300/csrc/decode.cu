@@ -48,6 +48,9 @@ constexpr int kMaxCtaPages = 1024;
 
 struct DecodeParams {
   int hkv, hq, G, sink, window, max_pages;
+  // query heads per CTA: the MMA tiles hold 8, so G = 16 is served as two halves
+  // of 8 query heads (each half reads the KV head's pages)
+  int gq, halves;
   int64_t n_int2_pages, n_bf16_pages;
   const uint8_t* int2_pool;
   const uint8_t* bf16_pool;
@@ -83,8 +86,9 @@ __global__ void __launch_bounds__(1024) qrot_kernel(const DecodeParams p) {
   pdl_trigger();
   __shared__ float qs[8][D];
   __shared__ float partial[1024 / D][8][D];
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int G = p.G;
+  const int h = blockIdx.x / p.halves, b = blockIdx.y, tid = threadIdx.x;
+  const int qh0 = h * p.G + (blockIdx.x % p.halves) * p.gq;   // first query head of this CTA
+  const int G = p.gq;
   constexpr int CH = 1024 / D;          // chunks of the contraction index
   constexpr int PER = D / CH;
   const int j = tid % D, c = tid / D;
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(1024) qrot_kernel(const DecodeParams p) {
 #pragma unroll
   for (int u = 0; u < PER; ++u) rv[u] = r[(c * PER + u) * D + j];
   for (int i = tid; i < G * D; i += blockDim.x)
-    qs[i / D][i % D] = bf16_to_float(p.q[(static_cast<size_t>(b) * p.hq + h * G) * D + i]);
+    qs[i / D][i % D] = bf16_to_float(p.q[(static_cast<size_t>(b) * p.hq + qh0) * D + i]);
   __syncthreads();
   for (int g = 0; g < G; ++g) {
     float acc = 0.f;
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(1024) qrot_kernel(const DecodeParams p) {
     float acc = 0.f;
 #pragma unroll
     for (int cc = 0; cc < CH; ++cc) acc += partial[cc][g][jj];
-    p.qrot[(static_cast<size_t>(b) * p.hq + h * G + g) * D + jj] = acc;
+    p.qrot[(static_cast<size_t>(b) * p.hq + qh0 + g) * D + jj] = acc;
   }
 }
 
@@ -345,11 +349,11 @@ template <int D, int NS>
 __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, int lo, int n, int L, uint8_t* ring,
                                            uint64_t* bars, uint2* qbs, float (&o)[D / 16][4],
-                                           float (&zacc)[4], Softmax& sm, int defer_lp) {
+                                           float (&zacc)[4], Softmax& sm, int defer_lp, int qh0) {
   static_assert(NS % 2 == 0, "pages are consumed in pairs of stages");
   constexpr int NG = D / 32, NK = D / 16;
   constexpr int SB = Fmt<D>::kInt2Block;
-  const int gid = lane >> 2, tig = lane & 3, G = p.G;
+  const int gid = lane >> 2, tig = lane & 3, G = p.gq;
   uint8_t* wring = ring + warp * NS * SB;
   uint64_t* wbar = bars + warp * 8;
   const uint8_t* pool_h = p.int2_pool + static_cast<size_t>(h) * SB;
@@ -377,7 +381,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
   pdl_wait();
   uint32_t qz = 0;
   {
-    const float* qr = p.qrot + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
+    const float* qr = p.qrot + (static_cast<size_t>(b) * p.hq + qh0 + gid) * D;
     float gs[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) gs[g] = 0.f;
@@ -486,10 +490,10 @@ template <int D, int NS>
 __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, const int* lps, int n, int L, int mode,
                                            uint8_t* ring, uint64_t* bars, float (&o)[D / 16][4],
-                                           Softmax& sm) {
+                                           Softmax& sm, int qh0) {
   constexpr int NK = D / 16;
   constexpr int SB = Fmt<D>::kBf16Block;
-  const int gid = lane >> 2, tig = lane & 3, G = p.G;
+  const int gid = lane >> 2, tig = lane & 3, G = p.gq;
   uint8_t* wring = ring + warp * NS * SB;
   uint64_t* wbar = bars + warp * 8;
   const uint8_t* pool_h = p.bf16_pool + static_cast<size_t>(h) * SB;
@@ -511,7 +515,7 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
   if (p.after_append) prefill();
   uint32_t qb[NK][2];
   {
-    const uint16_t* qr = p.q + (static_cast<size_t>(b) * p.hq + h * G + gid) * D;
+    const uint16_t* qr = p.q + (static_cast<size_t>(b) * p.hq + qh0 + gid) * D;
 #pragma unroll
     for (int kk = 0; kk < NK; ++kk) {
       qb[kk][0] = gid < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig) : 0u;
@@ -577,10 +581,11 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
   uint8_t* ring = smem + C::kRingOff;
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, h = blockIdx.y / p.halves, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int G = p.G;
+  const int G = p.gq;
+  const int qh0 = h * p.G + (blockIdx.y % p.halves) * p.gq;   // first query head of this CTA
 
   // Without a gate kernel in front (the BF16-only call), nothing may be read
   // before the predecessor grid completes.
@@ -657,9 +662,9 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   const int defer_lp = (p.after_append && L - 1 - p.window >= p.sink) ? (L - 1 - p.window) / kPage : -1;
   if (mode == 0)
     int2_pages<D, C::kStagesI>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
-                               reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp);
+                               reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp, qh0);
   else
-    bf16_pages<D, C::kStagesB>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm);
+    bf16_pages<D, C::kStagesB>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm, qh0);
 
   pdl_trigger();
 
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) Os = fmaf(esc[w * 8 + g], scr[w * (16 + 8 * D) + 16 + g * D + ch], Os);
     float* dst = p.part +
-                 ((static_cast<size_t>(b) * p.hq + h * G + g) * p.n_splits + split) * (D + 2);
+                 ((static_cast<size_t>(b) * p.hq + qh0 + g) * p.n_splits + split) * (D + 2);
     if (ch == 0) {
       float Ls = 0.f;
 #pragma unroll
@@ -880,7 +885,8 @@ Plan make_plan(const oscar_cache_desc* c, int batch, int max_len, bool bf16_only
   main_pages = std::max(main_pages, 1);
   const int per_sm = bf16_only ? SplitCfg<128, true>::kCtasPerSm : SplitCfg<128, false>::kCtasPerSm;
   // one wave: units * (main splits + the BF16 split) CTAs fill every resident slot
-  const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads;
+  const int g_all = c->num_q_heads / c->num_kv_heads;
+  const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * (g_all > 8 ? g_all / 8 : 1);
   const int64_t slots = static_cast<int64_t>(per_sm) * oscar_host::sm_count();
   int n_main = static_cast<int>(std::max<int64_t>(1, slots / units - (bf16_only ? 0 : 1)));
   n_main = std::min(n_main, main_pages);
@@ -916,14 +922,14 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
   using C = SplitCfg<D, kBf16Only>;
   if (!oscar_host::allow_smem(reinterpret_cast<const void*>(split_kernel<D, kBf16Only>), C::kBytes))
     return OSCAR_ERR_CUDA;
-  const dim3 sgrid(pl.n_splits, p.hkv, p.batch);
+  const dim3 sgrid(pl.n_splits, p.hkv * p.halves, p.batch);
   cudaError_t e;
   // every kernel is launched with programmatic stream serialisation: it may
   // start while its predecessor drains, and waits (griddepcontrol.wait) before
   // touching anything the predecessor produces
   if (!kBf16Only) {
     if (!p.after_append) {   // a fused step's append kernel has written q' already
-      e = launch_pdl(qrot_kernel<D>, dim3(p.hkv, p.batch), dim3(1024), 0, st, p);
+      e = launch_pdl(qrot_kernel<D>, dim3(p.hkv * p.halves, p.batch), dim3(1024), 0, st, p);
       if (e != cudaSuccess) return OSCAR_ERR_CUDA;
     }
     e = launch_pdl(split_kernel<D, kBf16Only>, sgrid, dim3(kDThreads), C::kBytes, st, p);
@@ -962,6 +968,8 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.hkv = c->num_kv_heads;
   p.hq = c->num_q_heads;
   p.G = c->num_q_heads / c->num_kv_heads;
+  p.gq = p.G < 8 ? p.G : 8;
+  p.halves = p.G / p.gq;
   p.sink = c->sink;
   p.window = c->window;
   p.max_pages = c->max_pages_per_seq;

@@ -117,12 +117,13 @@ def decode(cache, q, lens, max_len=None, bf16_only=False, out=None):
     return from_bf16(o)
 
 
-def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa):
+def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=None):
     """The oracle's attention over what the GPU actually stored: every token of
     every sequence read back from the pools (INT2 codes, s16, z16 dequantised and
     rotated back with R^T; BF16 tokens as stored), then fp64 softmax attention.
     Separates the decode kernels' parity from the quantiser's (whose flagged
-    near-boundary codes may differ from the oracle's by one step)."""
+    near-boundary codes may differ from the oracle's by one step).  ``drop``:
+    optional {sequence: logical pages} whose tokens are left out."""
     got2, gotb = pools(cache)
     B, Hq, d = q.shape
     hkv = Hq // gqa
@@ -155,7 +156,11 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa):
                     sl = slots[~mi]
                     k[ts[~mi]] = synth.bf16_from_bits(kb[sl])
                     v[ts[~mi]] = synth.bf16_from_bits(vb[sl])
-            out[b, h * gqa:(h + 1) * gqa] = attention.softmax_attention(q[b, h * gqa:(h + 1) * gqa], k, v)
+            keep = np.ones(L, bool)
+            for pg in (drop or {}).get(b, ()):
+                keep[16 * pg:16 * pg + 16] = False
+            out[b, h * gqa:(h + 1) * gqa] = attention.softmax_attention(q[b, h * gqa:(h + 1) * gqa],
+                                                                      k[keep], v[keep])
     return out
 
 

@@ -1,5 +1,9 @@
 """GPU parity of split-K decode attention over the mixed cache (and of the
-same-design BF16 baseline) against the oracle's plain-definition attention."""
+same-design BF16 baseline) against the oracle's plain-definition attention,
+computed from the codes the cache actually stores: the parity rule for the
+attention output.  The stored codes themselves are checked against the
+oracle's quantiser in test_quantize_gpu.py (bit-exact except flagged
+near-boundary entries, where one step either way is allowed)."""
 import numpy as np
 import pytest
 
@@ -26,20 +30,19 @@ def _run(wl, lens, W, *, n_calib=512, shared=0, permute=None, max_len=None, vari
     (synth.QWEN3_32B_128K, [5000, 1], 128),                    # G=8, L=1 edge
 ])
 def test_decode_matches_oracle(wl, lens, W):
-    inst, rot, cache, _, out = _run(wl, lens, W)
-    ref = attention.mixed_decode(inst.q, inst.k, inst.v, inst.seq_lens, rot, sink=4, window=W,
+    inst, rot, cache, pp, out = _run(wl, lens, W)
+    ref = H.attention_from_pools(cache, pp, inst.q, inst.seq_lens, rot, sink=4, window=W,
                                  gqa=wl.gqa)
     H.check_close(out, ref, f"{wl.name} {lens}")
     assert H.status(cache) == 0
 
 
-@pytest.mark.parametrize("g", [1, 2])
+@pytest.mark.parametrize("g", [1, 2, 16])
 def test_small_gqa_groups(g):
     wl = synth.Workload("g%d" % g, batch=2, num_q_heads=2 * g, num_kv_heads=2, head_dim=128,
                         context=3000, n_calib=256)
-    inst, rot, cache, _, out = _run(wl, [3000, 1777], 128)
-    ref = attention.mixed_decode(inst.q, inst.k, inst.v, inst.seq_lens, rot, sink=4, window=128,
-                                 gqa=g)
+    inst, rot, cache, pp, out = _run(wl, [3000, 1777], 128)
+    ref = H.attention_from_pools(cache, pp, inst.q, inst.seq_lens, rot, sink=4, window=128, gqa=g)
     H.check_close(out, ref)
 
 
@@ -86,7 +89,7 @@ def test_prefix_sharing_equals_private_copies():
     H.prefill(c2, inst)
     o2 = H.decode(c2, inst.q, inst.seq_lens)
     np.testing.assert_array_equal(o1, o2)
-    ref = attention.mixed_decode(inst.q, inst.k, inst.v, inst.seq_lens, rot, sink=4, window=128,
+    ref = H.attention_from_pools(c1, pp1, inst.q, inst.seq_lens, rot, sink=4, window=128,
                                  gqa=wl.gqa)
     H.check_close(o1, ref)
 
@@ -121,8 +124,7 @@ def test_bad_lengths_are_reported_not_faulted():
     t.cuda.synchronize()
     assert H.status(cache) & L.DEVERR_SEQ_LEN
     assert float(o[1].float().abs().max()) == 0.0
-    ref = attention.mixed_decode(inst.q[:1], inst.k[:1], inst.v[:1], [300], rot, sink=4, window=64,
-                                 gqa=4)
+    ref = H.attention_from_pools(cache, pp, inst.q[:1], [300], rot, sink=4, window=64, gqa=4)
     H.check_close(H.from_bf16(o)[:1], ref)
 
 
@@ -141,13 +143,6 @@ def test_bad_page_id_is_masked_and_reported():
     cache.int2_page_table = t.from_numpy(tbl).to(H.DEV)
     out = H.decode(cache, inst.q, inst.seq_lens)
     assert H.status(cache) & H.lib().DEVERR_PAGE_ID
-    keep = np.ones(2500, bool)
-    keep[16 * bad_page:16 * bad_page + 16] = False
-    ref = np.zeros_like(out)
-    for h in range(wl.num_kv_heads):
-        ke, ve = attention.effective_kv(inst.k[0][h], inst.v[0][h], 2500, 4, 128, rot.rk[h],
-                                        rot.rv[h], rot.ck[h], rot.cv[h])
-        G = wl.gqa
-        ref[0, h * G:(h + 1) * G] = attention.softmax_attention(inst.q[0, h * G:(h + 1) * G],
-                                                                ke[keep], ve[keep])
+    ref = H.attention_from_pools(cache, pp, inst.q, [2500], rot, sink=4, window=128, gqa=wl.gqa,
+                                 drop={0: [bad_page]})
     H.check_close(out, ref)
