@@ -601,6 +601,40 @@ def extra_prefix(dev, l2, n_calib):
     return res
 
 
+def extra_multiquery(dev, l2, n_calib, rows=16):
+    """Several query rows per sequence (a chunk of new tokens at the end of a
+    32768-token Qwen3-8B cache) through oscar_multiquery_attention."""
+    torch = __import__("torch")
+    from int2_rotated_kv_gb300 import _lib as L
+    w = synth.QWEN3_8B_32K
+    di = synth.draw_device(w, w.seq_lens(), dev, n_calib=n_calib)
+    rot = calibrate_with_library(di, n_calib)
+    dec = Decoder(di, rot, dev, l2_bytes=l2)
+    Lc = int(dec.lens[0])
+    pos = torch.arange(Lc - rows, Lc, dtype=torch.int32, device=dev)[None]
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    q = torch.randn((1, rows, w.num_q_heads, w.head_dim), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    ws = torch.empty(L.oscar_decode_workspace_size(dec.caches[0], rows, Lc) // 4 + 64,
+                     dtype=torch.float32, device=dev)
+    # the caches hold L-1 tokens until a step runs; one step fills the last slot
+    for i in range(dec.n_layers):
+        dec.step(i)
+    torch.cuda.synchronize()
+
+    def call(i):
+        L.oscar_multiquery_attention(dec.caches[i % dec.n_layers], q, dec.lens_dev, pos, Lc, out, ws)
+    t = time_graph(dec, call, 200, 10)
+    unique = attention_bytes(dec.lens, w.num_kv_heads, w.num_q_heads, w.head_dim, w.sink, w.window)
+    res = {"rows": rows, "us_per_call": round(t * 1e3, 3), "rows_per_s": round(rows / (t * 1e-3), 1),
+           "unique_GBps": round(unique / t / 1e6, 1), "read_GBps": round(rows * unique / t / 1e6, 1),
+           "note": "each row reads its sequence's pages"}
+    del dec
+    torch.cuda.empty_cache()
+    return res
+
+
 def pool_bytes_per_seq(w, L, bf16_only):
     """Allocated page-slot bytes of one sequence of L tokens in one layer (the
     same page plan the decoder allocates: cache filled to L - 1 plus one page of growth)."""
@@ -797,7 +831,7 @@ def main():
         del dec
         torch.cuda.empty_cache()
         legs = ((synth.QWEN3_32B_128K.name, extra_long), (synth.QWEN3_4B_PREFIX.name, extra_prefix),
-                (synth.QWEN3_8B_BUDGET.name, extra_budget))
+                (synth.QWEN3_8B_BUDGET.name, extra_budget), ("qwen3_8b_32k_chunk16", extra_multiquery))
         for name, fn in legs:
             try:
                 ex[name] = fn(dev, l2, 2048)

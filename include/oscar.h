@@ -182,6 +182,28 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
                                          int32_t max_seq_len, void* out, void* workspace,
                                          size_t workspace_bytes, void* stream);
 
+/* Attention for several query rows per sequence over the mixed cache: a chunk
+ * of new tokens (chunked prefill after a prefix-cache hit) or tokens to verify
+ * ("Technical Summary: OSCAR ...", section 2.2B: compatibility with paged KV
+ * serving and prefix caching).  The cache holds seq_lens[b] tokens of sequence
+ * b, the rows' own tokens included (placed beforehand with
+ * oscar_prefill_quantize or oscar_quantize_append), in the form a sequence of
+ * that length stores them; row m of sequence b attends to the stored tokens at
+ * positions 0 .. q_pos[b * m_rows + m] (causal).
+ *   q, out:  bf16 [batch][m_rows][Hq][d], device.
+ *   q_pos:   int32 [batch][m_rows], device.  A position outside
+ *            [0, seq_lens[b]) gives a zero output row and sets
+ *            OSCAR_DEVERR_SEQ_LEN in desc->status.
+ *   workspace: oscar_decode_workspace_size(desc, batch * m_rows, max_seq_len)
+ *            bytes, no initial contents required.
+ * Each row reads its sequence's pages (rows of one sequence do not share the
+ * page reads).  Asynchronous. */
+oscar_status oscar_multiquery_attention(const oscar_cache_desc* desc, const void* q,
+                                        const int32_t* seq_lens, const int32_t* q_pos,
+                                        int32_t batch, int32_t m_rows, int32_t max_seq_len,
+                                        void* out, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* One decode step over the mixed cache: oscar_quantize_append (the new token
  * into its BF16 slot, the token leaving the recent window rotated, clipped,
  * quantised and packed into its INT2 slot) followed by oscar_decode_attention

@@ -25,7 +25,7 @@ EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rot
             "oscar_prefill_quantize", "oscar_quantize_append", "oscar_decode_workspace_size",
             "oscar_decode_attention", "oscar_decode_attention_bf16", "oscar_device_sm_count",
             "oscar_status_string", "oscar_version", "oscar_decode_attention_static",
-            "oscar_decode_step")
+            "oscar_decode_step", "oscar_multiquery_attention")
 
 
 class OscarError(RuntimeError):
@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "oscar_device_sm_count": (I32, []),
             "oscar_decode_attention_static": (I32, [P, P, P, I32, I32, P, P]),
             "oscar_decode_step": (I32, [P, P, P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
+            "oscar_multiquery_attention": (I32, [P, P, P, P, I32, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_status_string": (ctypes.c_char_p, [I32]),
             "oscar_version": (I32, []),
         }
@@ -240,6 +241,19 @@ def oscar_decode_step(cache: Cache, q, k_new, v_new, seq_lens_after, max_seq_len
                                    _ptr(seq_lens_after), int(seq_lens_after.numel()),
                                    int(max_seq_len), _ptr(out), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def oscar_multiquery_attention(cache: Cache, q, seq_lens, q_pos, max_seq_len: int, out, workspace,
+                               stream=None):
+    """Several query rows per sequence (q [B][M][Hq][d], q_pos [B][M]) over the
+    mixed cache; row (b, m) attends to stored tokens 0 .. q_pos[b][m]."""
+    d = cache.desc()
+    B, M = int(q_pos.shape[0]), int(q_pos.shape[1])
+    _check("oscar_multiquery_attention",
+           lib().oscar_multiquery_attention(ctypes.byref(d), _ptr(q), _ptr(seq_lens), _ptr(q_pos),
+                                            B, M, int(max_seq_len), _ptr(out), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream(stream)))
 
 
 def oscar_decode_attention_static(cache: Cache, q, seq_lens, max_seq_len: int, out, stream=None):

@@ -74,6 +74,10 @@ struct DecodeParams {
   // pages that kernel writes -- the INT2 page of the token leaving the window,
   // the BF16 page of the new token -- are copied only after griddepcontrol.wait
   int after_append;
+  // several query rows per sequence: row b of the batch belongs to sequence
+  // b / rows_per_seq and sees stored tokens 0 .. limits[b] only (null: decode)
+  int rows_per_seq;
+  const int32_t* limits;
 };
 
 // ------------------------------------------------------------------ q R_K
@@ -212,10 +216,11 @@ __device__ __forceinline__ void softmax_pair(Softmax& st, float (&la)[4], float 
   pb[2] = fast_exp2(lb[2] - b0); pb[3] = fast_exp2(lb[3] - b1);
 }
 
-__device__ __forceinline__ bool tok_ok(int t, int L, int sink, int window, int mode) {
-  // mode 0: INT2 region; 1: BF16 region (sink + recent); 2: all tokens
-  if (mode == 0) return t >= sink && t < L - window;
-  if (mode == 1) return t < L && (t < sink || t >= L - window);
+__device__ __forceinline__ bool tok_ok(int t, int L, int sink, int window, int mode, int lim) {
+  // mode 0: INT2 region; 1: BF16 region (sink + recent); 2: all tokens; lim: the
+  // row sees positions below lim only (lim <= L)
+  if (mode == 0) return t >= sink && t < L - window && t < lim;
+  if (mode == 1) return t < lim && (t < sink || t >= L - window);
   return t < L;
 }
 
@@ -349,7 +354,8 @@ template <int D, int NS>
 __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, int lo, int n, int L, uint8_t* ring,
                                            uint64_t* bars, uint2* qbs, float (&o)[D / 16][4],
-                                           float (&zacc)[4], Softmax& sm, int defer_lp, int qh0) {
+                                           float (&zacc)[4], Softmax& sm, int defer_lp, int qh0,
+                                           int lim) {
   static_assert(NS % 2 == 0, "pages are consumed in pairs of stages");
   constexpr int NG = D / 32, NK = D / 16;
   constexpr int SB = Fmt<D>::kInt2Block;
@@ -428,7 +434,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     }
   }
   const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
-  const int tok_lo = p.sink, tok_hi = L - p.window;
+  const int tok_lo = p.sink, tok_hi = min(L - p.window, lim);
   uint32_t phase = 0;
   int s = 0;
   int i = 0;
@@ -486,11 +492,15 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
 
 // BF16 pages (the sink + recent split, or every page of the BF16 baseline):
 // raw q against bf16 keys and values in the same fragment-native order.
-template <int D, int NS>
+// kSplitP: the probabilities enter p.V as a bf16 pair (p = hi + lo, two MMAs),
+// so the weights are exact to ~2^-17 instead of bf16's 2^-9.  Used for the
+// sink + recent split of the mixed cache, where a query row may see only a few
+// tokens (a row early in a chunk); the all-BF16 baseline keeps one MMA.
+template <int D, int NS, bool kSplitP = false>
 __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, const int* lps, int n, int L, int mode,
                                            uint8_t* ring, uint64_t* bars, float (&o)[D / 16][4],
-                                           Softmax& sm, int qh0) {
+                                           Softmax& sm, int qh0, int lim) {
   constexpr int NK = D / 16;
   constexpr int SB = Fmt<D>::kBf16Block;
   const int gid = lane >> 2, tig = lane & 3, G = p.gq;
@@ -540,21 +550,33 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
       }
       float lg[4] = {dk[0] * scale_log2, dk[1] * scale_log2, dk[2] * scale_log2, dk[3] * scale_log2};
       const int pbeg = lps[k] * kPage;
-      const bool whole = mode == 2 && pbeg + kPage <= L;
+      const bool whole = mode == 2 && pbeg + kPage <= L && p.limits == nullptr;
       if (!whole) {
         const int t0 = pbeg + gid, t1 = t0 + 8;
-        if (!tok_ok(t0, L, p.sink, p.window, mode)) lg[0] = lg[1] = -INFINITY;
-        if (!tok_ok(t1, L, p.sink, p.window, mode)) lg[2] = lg[3] = -INFINITY;
+        if (!tok_ok(t0, L, p.sink, p.window, mode, lim)) lg[0] = lg[1] = -INFINITY;
+        if (!tok_ok(t1, L, p.sink, p.window, mode, lim)) lg[2] = lg[3] = -INFINITY;
       }
       float pr[4];
       softmax_tile<NK>(sm, lg, o, zdummy, pr);
-      const uint32_t pb0 = movmatrix_trans(pack_bf162(pr[0], pr[1]));
-      const uint32_t pb1 = movmatrix_trans(pack_bf162(pr[2], pr[3]));
+      const uint32_t h01 = pack_bf162(pr[0], pr[1]);
+      const uint32_t h23 = pack_bf162(pr[2], pr[3]);
+      const uint32_t pb0 = movmatrix_trans(h01);
+      const uint32_t pb1 = movmatrix_trans(h23);
       const uint4* vb = reinterpret_cast<const uint4*>(st + Fmt<D>::kBf16V);
 #pragma unroll
       for (int mt = 0; mt < NK; ++mt) {
         const uint4 a = vb[mt * 32 + lane];
         mma_bf16(o[mt], a.x, a.y, a.z, a.w, pb0, pb1);
+      }
+      if constexpr (kSplitP) {
+        // the part of p the bf16 rounding dropped
+        const uint32_t pl0 = movmatrix_trans(pack_bf162(pr[0] - bf16_lo_value(h01), pr[1] - bf16_hi_value(h01)));
+        const uint32_t pl1 = movmatrix_trans(pack_bf162(pr[2] - bf16_lo_value(h23), pr[3] - bf16_hi_value(h23)));
+#pragma unroll
+        for (int mt = 0; mt < NK; ++mt) {
+          const uint4 a = vb[mt * 32 + lane];
+          mma_bf16(o[mt], a.x, a.y, a.z, a.w, pl0, pl1);
+        }
       }
     }
     __syncwarp();
@@ -596,7 +618,8 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   const int mode = kBf16Only ? 2 : (bf16_split ? 1 : 0);
   const int first = mode == 0 ? p.sink / kPage : 0;
   const int lo = first + split * p.pps;
-  const int32_t* pt = (mode == 0 ? p.int2_pt : p.bf16_pt) + static_cast<size_t>(b) * p.max_pages;
+  const int sb = b / p.rows_per_seq;   // the sequence this row reads
+  const int32_t* pt = (mode == 0 ? p.int2_pt : p.bf16_pt) + static_cast<size_t>(sb) * p.max_pages;
   const int64_t npages = mode == 0 ? p.n_int2_pages : p.n_bf16_pages;
   int spec[(kMaxCtaPages + kDThreads - 1) / kDThreads];
   if (mode != 1) {
@@ -606,10 +629,21 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
       spec[r] = (k < p.pps && lo + k < p.max_pages) ? pt[lo + k] : -1;
     }
   }
-  int L = p.seq_lens[b];
+  int L = p.seq_lens[sb];
   if (L < 1 || L > p.max_len) {
     if (tid == 0 && p.status) atomicOr(p.status, OSCAR_DEVERR_SEQ_LEN);
     L = 0;
+  }
+  // visibility limit of this row: positions below lim (the whole cache for a decode)
+  int lim = L;
+  if (p.limits) {
+    const int qp = p.limits[b];
+    if (qp < 0 || qp >= L) {
+      if (tid == 0 && p.status && L > 0) atomicOr(p.status, OSCAR_DEVERR_SEQ_LEN);
+      lim = 0;
+    } else {
+      lim = qp + 1;
+    }
   }
   int n = 0;
   if (mode == 1) {
@@ -631,8 +665,9 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
       ids[k] = id;
     }
   } else {
+    const int hi = min(L - p.window, lim);   // INT2 tokens this row sees end below hi
     const int last = mode == 0
-        ? ((L - p.window > p.sink) ? (L - p.window + kPage - 1) / kPage : first)
+        ? ((hi > p.sink) ? (hi + kPage - 1) / kPage : first)
         : (L + kPage - 1) / kPage;
     n = max(0, min(min(last, lo + p.pps) - lo, kMaxCtaPages));
 #pragma unroll
@@ -662,9 +697,10 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   const int defer_lp = (p.after_append && L - 1 - p.window >= p.sink) ? (L - 1 - p.window) / kPage : -1;
   if (mode == 0)
     int2_pages<D, C::kStagesI>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
-                               reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp, qh0);
+                               reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp, qh0, lim);
   else
-    bf16_pages<D, C::kStagesB>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm, qh0);
+    bf16_pages<D, C::kStagesB, !kBf16Only>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm, qh0,
+                               lim);
 
   pdl_trigger();
 
@@ -948,7 +984,8 @@ oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, cons
 oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_t* seq_lens,
                           int batch, int max_len, void* out, void* ws, size_t ws_bytes,
                           void* stream, bool bf16_only, const void* k_new = nullptr,
-                          const void* v_new = nullptr) {
+                          const void* v_new = nullptr, const int32_t* limits = nullptr,
+                          int rows_per_seq = 1) {
   oscar_status s = oscar_host::check_desc(c, !bf16_only, true);
   if (s != OSCAR_OK) return s;
   if (batch < 0 || max_len < 1) return OSCAR_ERR_INVALID_ARG;
@@ -985,7 +1022,9 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
   p.seq_lens = seq_lens;
-  p.batch = batch;
+  p.batch = batch;   // rows: sequences x rows_per_seq
+  p.rows_per_seq = rows_per_seq;
+  p.limits = limits;
   p.max_len = max_len;
   p.n_main = pl.n_main;
   p.pps = pl.pps;
@@ -1097,6 +1136,17 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
 }
 
 int32_t oscar_device_sm_count(void) { return oscar_host::sm_count(); }
+
+oscar_status oscar_multiquery_attention(const oscar_cache_desc* desc, const void* q,
+                                        const int32_t* seq_lens, const int32_t* q_pos,
+                                        int32_t batch, int32_t m_rows, int32_t max_seq_len,
+                                        void* out, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  if (batch < 0 || m_rows < 1 || !q_pos) return OSCAR_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * m_rows > (int64_t(1) << 30)) return OSCAR_ERR_INVALID_ARG;
+  return oscar::decode_entry(desc, q, seq_lens, batch * m_rows, max_seq_len, out, workspace,
+                             workspace_bytes, stream, false, nullptr, nullptr, q_pos, m_rows);
+}
 
 oscar_status oscar_decode_step(const oscar_cache_desc* desc, const void* q, const void* k_new,
                                const void* v_new, const int32_t* seq_lens_after, int32_t batch,

@@ -90,6 +90,27 @@ def mixed_decode(q: np.ndarray, k: list, v: list, lens, rot: "cache.Rotations", 
     return out
 
 
+def mixed_multiquery(q: np.ndarray, k: list, v: list, lens, q_pos, rot: "cache.Rotations", *,
+                     sink: int, window: int, gqa: int) -> np.ndarray:
+    """Several query rows per sequence over the mixed cache (a chunk of new
+    tokens, or tokens to verify): out [B, M, Hq, d] for q [B, M, Hq, d].  The
+    cache holds L_b tokens in the form a sequence of length L_b stores them
+    (BF16 sink and recent window, INT2 in between); row m of sequence b attends
+    to the stored tokens at positions 0 .. q_pos[b][m] (causal)."""
+    B, M, Hq, d = q.shape
+    out = np.zeros((B, M, Hq, d))
+    for b in range(B):
+        L = int(lens[b])
+        for h in range(Hq // gqa):
+            ke, ve = effective_kv(k[b][h], v[b][h], L, sink, window,
+                                  rot.rk[h], rot.rv[h], rot.ck[h], rot.cv[h])
+            for m in range(M):
+                n = int(q_pos[b][m]) + 1
+                out[b, m, h * gqa:(h + 1) * gqa] = softmax_attention(q[b, m, h * gqa:(h + 1) * gqa],
+                                                                     ke[:n], ve[:n])
+    return out
+
+
 def bf16_decode(q: np.ndarray, k: list, v: list, lens, *, gqa: int) -> np.ndarray:
     """All-BF16 cache: plain softmax attention over the stored bf16 values."""
     B, Hq, d = q.shape

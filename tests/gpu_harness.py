@@ -117,13 +117,14 @@ def decode(cache, q, lens, max_len=None, bf16_only=False, out=None):
     return from_bf16(o)
 
 
-def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=None):
+def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=None, upto=None):
     """The oracle's attention over what the GPU actually stored: every token of
     every sequence read back from the pools (INT2 codes, s16, z16 dequantised and
     rotated back with R^T; BF16 tokens as stored), then fp64 softmax attention.
     Separates the decode kernels' parity from the quantiser's (whose flagged
     near-boundary codes may differ from the oracle's by one step).  ``drop``:
-    optional {sequence: logical pages} whose tokens are left out."""
+    optional {sequence: logical pages} whose tokens are left out.  ``upto``:
+    optional last visible position per sequence (a query row of a chunk)."""
     got2, gotb = pools(cache)
     B, Hq, d = q.shape
     hkv = Hq // gqa
@@ -159,6 +160,8 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=Non
             keep = np.ones(L, bool)
             for pg in (drop or {}).get(b, ()):
                 keep[16 * pg:16 * pg + 16] = False
+            if upto is not None:
+                keep[int(upto[b]) + 1:] = False
             out[b, h * gqa:(h + 1) * gqa] = attention.softmax_attention(q[b, h * gqa:(h + 1) * gqa],
                                                                       k[keep], v[keep])
     return out

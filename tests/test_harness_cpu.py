@@ -48,3 +48,25 @@ def test_attention_from_pools_drops_whole_pages():
     keep[80:96] = False
     ref = attention.softmax_attention(inst.q[0, 0:4], ke[keep], ve[keep])
     np.testing.assert_allclose(got[0, 0:4], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_from_pools_upto_matches_multiquery_oracle():
+    """A visibility limit per sequence reproduces the oracle's multi-row attention."""
+    import torch
+    wl = synth.TINY
+    lens = np.array([300, 250])
+    inst = synth.draw_instance(wl, n_calib=256, seq_lens=lens)
+    rot = attention.calibrate(inst.calib_q, inst.calib_k, inst.calib_v, 0)
+    pp = pages.plan(lens, 4, 64)
+    exp = ocache.expected_pools(inst.k, inst.v, lens, rot, sink=4, window=64, d=wl.head_dim,
+                                hkv=1, int2_table=pp.int2_table, bf16_table=pp.bf16_table,
+                                num_int2_pages=pp.num_int2_pages, num_bf16_pages=pp.num_bf16_pages)
+    cache = types.SimpleNamespace(int2_pool=torch.from_numpy(exp.int2.copy()),
+                                  bf16_pool=torch.from_numpy(exp.bf16.view(np.int16).copy()).view(torch.bfloat16))
+    pos = np.array([[120, 299], [7, 249]])
+    q = np.stack([inst.q, inst.q], axis=1)                    # [B, M, Hq, d]
+    ref = attention.mixed_multiquery(q, inst.k, inst.v, lens, pos, rot, sink=4, window=64, gqa=4)
+    for m in range(2):
+        got = H.attention_from_pools(cache, pp, q[:, m], lens, rot, sink=4, window=64, gqa=4,
+                                     upto=pos[:, m])
+        np.testing.assert_allclose(got, ref[:, m], rtol=1e-12, atol=1e-12)

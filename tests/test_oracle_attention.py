@@ -125,3 +125,52 @@ def test_expected_pools_roundtrip_and_prefix_sharing():
     np.testing.assert_array_equal(exp.int2_defined[:blk], tb['owner'] >= S)   # page 0: sink slots unused
     bk, bv = layout.unpack_bf16_block(exp.bf16[:32 * d], d)
     np.testing.assert_array_equal(bk[:S], synth.bf16_bits(shared_k[:S]))
+
+
+# --------------------------------------------------------- several query rows
+
+def test_multiquery_single_row_at_the_end_is_decode():
+    """One row per sequence at position L - 1 is exactly the decode attention."""
+    inst = synth.draw_instance(synth.TINY, n_calib=128, seq_lens=[300, 200])
+    rot = attention.calibrate(inst.calib_q, inst.calib_k, inst.calib_v, 0)
+    q4 = inst.q[:, None]
+    got = attention.mixed_multiquery(q4, inst.k, inst.v, inst.seq_lens,
+                                     [[L - 1] for L in inst.seq_lens], rot, sink=4, window=64,
+                                     gqa=4)
+    ref = attention.mixed_decode(inst.q, inst.k, inst.v, inst.seq_lens, rot, sink=4, window=64,
+                                 gqa=4)
+    np.testing.assert_array_equal(got[:, 0], ref)
+
+
+def test_multiquery_all_bf16_is_causal_attention_by_loops():
+    """Identity rotation with the window covering the context: row m attends to
+    tokens 0 .. q_pos (causal), checked against explicit loops."""
+    rng = np.random.default_rng(5)
+    L, d, G, M = 40, 8, 2, 4
+    k = [[rng.standard_normal((L, d))]]
+    v = [[rng.standard_normal((L, d))]]
+    q = rng.standard_normal((1, M, G, d))
+    pos = [[36, 37, 38, 39]]
+    eye = np.eye(d, dtype=np.float32)
+    rot = cache.Rotations([eye], [eye], [np.float32(1)], [np.float32(1)])
+    got = attention.mixed_multiquery(q, k, v, [L], pos, rot, sink=0, window=L, gqa=G)
+    for m in range(M):
+        n = pos[0][m] + 1
+        ref = attention.softmax_attention_loops(q[0, m], k[0][0][:n], v[0][0][:n])
+        np.testing.assert_allclose(got[0, m], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_multiquery_ignores_tokens_after_the_row():
+    """Changing tokens after a row's position changes nothing for that row."""
+    inst = synth.draw_instance(synth.TINY, n_calib=128, seq_lens=[300])
+    rot = attention.calibrate(inst.calib_q, inst.calib_k, inst.calib_v, 0)
+    q = np.stack([inst.q[0], inst.q[0]])[None]          # two rows, same query
+    pos = [[250, 299]]
+    a = attention.mixed_multiquery(q, inst.k, inst.v, [300], pos, rot, sink=4, window=64, gqa=4)
+    k2 = [[inst.k[0][0].copy()]]
+    v2 = [[inst.v[0][0].copy()]]
+    k2[0][0][260:] += 3.0
+    v2[0][0][260:] -= 2.0
+    b = attention.mixed_multiquery(q, k2, v2, [300], pos, rot, sink=4, window=64, gqa=4)
+    np.testing.assert_array_equal(a[0, 0], b[0, 0])      # row at 250 does not see 260..
+    assert np.abs(a[0, 1] - b[0, 1]).max() > 1e-3       # row at 299 does
