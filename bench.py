@@ -635,6 +635,72 @@ def extra_multiquery(dev, l2, n_calib, rows=16):
     return res
 
 
+def calib_attention_flops(n, hq, d):
+    """Useful FLOPs of causal calibration attention: query t meets t + 1 keys,
+    2d FLOPs for its logit and 2d for its share of P V."""
+    return 4.0 * d * hq * n * (n + 1) / 2
+
+
+def extra_calibration(dev, l2, n_calib=8192):
+    """Device calibration of one Qwen3-8B layer (32/8 heads, d = 128, 8192
+    calibration tokens): C_Q, C_S, then the clips of K and V under the R the
+    host builds from them."""
+    torch = __import__("torch")
+    from int2_rotated_kv_gb300 import _lib as L
+    w = synth.QWEN3_8B_32K
+    inst = synth.draw_instance(w, n_calib=n_calib, seq_lens=[1])
+    hkv, hq, d, G = w.num_kv_heads, w.num_q_heads, w.head_dim, w.gqa
+    q = np.zeros((n_calib, hq, d), np.float32)
+    for h in range(hkv):
+        q[:, h * G:(h + 1) * G] = inst.calib_q[h]
+    qd = bf16_dev(q, dev)
+    kd = bf16_dev(np.stack(inst.calib_k, axis=1), dev)
+    vd = bf16_dev(np.stack(inst.calib_v, axis=1), dev)
+    ws = torch.empty(L.oscar_calibration_workspace_size(hkv, hq, d, n_calib) // 4 + 64,
+                     dtype=torch.float32, device=dev)
+    cq = torch.empty((hkv, d, d), dtype=torch.float64, device=dev)
+    cs = torch.empty_like(cq)
+    ck = torch.empty(hkv, dtype=torch.float32, device=dev)
+    cv = torch.empty_like(ck)
+
+    def timed(fn, reps=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    t_q = timed(lambda: L.oscar_query_covariance_device(qd, hkv, cq, ws))
+    t_s = timed(lambda: L.oscar_score_covariance_device(qd, kd, vd, cs, ws))
+    t0 = time.perf_counter()
+    cq_h, cs_h = cq.cpu().numpy(), cs.cpu().numpy()
+    rk = np.stack([L.oscar_build_rotation(cq_h[h], inst.calib_k[h][:1], 99.9)[1] for h in range(hkv)])
+    rv = np.stack([L.oscar_build_rotation(cs_h[h], inst.calib_v[h][:1], 99.9)[1] for h in range(hkv)])
+    t_eig = time.perf_counter() - t0
+    rkd = torch.from_numpy(rk).to(dev)
+    rvd = torch.from_numpy(rv).to(dev)
+    t_c = timed(lambda: (L.oscar_clip_threshold_device(kd, rkd, 99.9, ck, ws),
+                         L.oscar_clip_threshold_device(vd, rvd, 99.9, cv, ws)))
+    fl = calib_attention_flops(n_calib, hq, d)
+    q_bytes = n_calib * hq * d * 2
+    res = {"n_calib": n_calib, "shape": f"{hq}/{hkv} heads, d={d}",
+           "query_covariance_ms": round(t_q, 4),
+           "query_covariance_GBps": round(q_bytes / t_q / 1e6, 1),
+           "score_covariance_ms": round(t_s, 4),
+           "score_attention_useful_TFLOPs": round(fl / t_s / 1e9, 1),
+           "clip_k_and_v_ms": round(t_c, 4),
+           "host_eigendecomposition_s": round(t_eig, 3),
+           "device_total_ms": round(t_q + t_s + t_c, 3)}
+    del ws, qd, kd, vd
+    torch.cuda.empty_cache()
+    return res
+
+
 def pool_bytes_per_seq(w, L, bf16_only):
     """Allocated page-slot bytes of one sequence of L tokens in one layer (the
     same page plan the decoder allocates: cache filled to L - 1 plus one page of growth)."""
@@ -831,7 +897,8 @@ def main():
         del dec
         torch.cuda.empty_cache()
         legs = ((synth.QWEN3_32B_128K.name, extra_long), (synth.QWEN3_4B_PREFIX.name, extra_prefix),
-                (synth.QWEN3_8B_BUDGET.name, extra_budget), ("qwen3_8b_32k_chunk16", extra_multiquery))
+                (synth.QWEN3_8B_BUDGET.name, extra_budget), ("qwen3_8b_32k_chunk16", extra_multiquery),
+                ("qwen3_8b_calibration_8192", extra_calibration))
         for name, fn in legs:
             try:
                 ex[name] = fn(dev, l2, 2048)

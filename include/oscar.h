@@ -241,6 +241,56 @@ oscar_status oscar_decode_attention_static(const oscar_cache_desc* desc, const v
                                            const int32_t* seq_lens, int32_t batch,
                                            int32_t max_seq_len, void* out, void* stream);
 
+/* ------------------------------------------------- calibration on the device
+ *
+ * The three statistics the offline step gathers per layer [Summary 2.1],
+ * [Summary 2.2A.1, 2.2A.4], computed on the GPU for long calibration sets and
+ * many layers; the eigendecomposition stays on the host (oscar_build_rotation
+ * takes the fp64 C these calls write).  Calibration tokens are one causal
+ * sequence of n tokens in the prefill's token-major layout:
+ *   q: device bf16 [n][num_q_heads][d]; k, v, x: device bf16 [n][num_kv_heads][d].
+ * Shapes: d in {64, 128}, G = num_q_heads / num_kv_heads in {1, 2, 4, 8, 16},
+ * 1 <= n <= 2^24 (else OSCAR_ERR_UNSUPPORTED / INVALID_ARG).  Pointers 16-byte
+ * aligned.  The calls are asynchronous on `stream`, allocate nothing and use
+ * the caller's workspace of at least oscar_calibration_workspace_size() bytes
+ * (one size serves all three calls; calls sharing a workspace must not overlap
+ * on the GPU).  Precision: bf16 inputs, products exact in fp32, fp32
+ * accumulation over at most 128 rows before a compensated (two-float) running
+ * sum; the result is rounded to fp64 (covariances) or fp32 (clip) at the end. */
+
+/* Workspace bytes for the calibration calls of one layer; 0 for an unsupported
+ * shape.  Depends on the current device's SM count. */
+size_t oscar_calibration_workspace_size(int32_t num_kv_heads, int32_t num_q_heads, int32_t d,
+                                        int64_t n);
+
+/* C_Q for every KV head [Summary 2.1 keys, 2.2A.1]: c_out[h] = (1/(n G))
+ * sum_t sum_{g<G} q[t][hG+g]^T q[t][hG+g] (the G query heads that read KV head
+ * h pooled).  c_out: device fp64 [num_kv_heads][d][d]. */
+oscar_status oscar_query_covariance_device(int32_t num_kv_heads, int32_t num_q_heads, int32_t d,
+                                           int64_t n, const void* q, double* c_out,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* C_S for every KV head [Summary 2.1 values, 2.2A.1]: for each query head
+ * hq = hG+g, O = S V with S the causal softmax(q_hq k_h^T / sqrt(d))
+ * probabilities over the calibration sequence; c_out[h] = (1/(n G)) sum_g O^T O.
+ * O is formed in fp32 with the probabilities carried as a bf16 (hi, lo) pair
+ * and kept in the workspace as a bf16 (hi, lo) pair.  c_out: device fp64
+ * [num_kv_heads][d][d]. */
+oscar_status oscar_score_covariance_device(int32_t num_kv_heads, int32_t num_q_heads, int32_t d,
+                                           int64_t n, const void* q, const void* k, const void* v,
+                                           double* c_out, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+
+/* Clip per KV head [Summary 2.2A.4]: clip_out[h] = the `percentile` (0..100,
+ * linear interpolation between order statistics, as oscar_build_rotation) of
+ * |x[:, h, :] R_h| over all n*d entries, with y = x R_h formed in fp32
+ * (sequential FMA over the input channel) and the order statistics selected
+ * exactly among those fp32 values.  r: device fp32 [num_kv_heads][d][d] (the
+ * cache's r_k or r_v); clip_out: device fp32 [num_kv_heads]. */
+oscar_status oscar_clip_threshold_device(int32_t num_kv_heads, int32_t d, int64_t n, const void* x,
+                                         const float* r, double percentile, float* clip_out,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* Number of SMs the split heuristics assume for the current device (>= 1). */
 int32_t oscar_device_sm_count(void);
 

@@ -25,7 +25,9 @@ EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rot
             "oscar_prefill_quantize", "oscar_quantize_append", "oscar_decode_workspace_size",
             "oscar_decode_attention", "oscar_decode_attention_bf16", "oscar_device_sm_count",
             "oscar_status_string", "oscar_version", "oscar_decode_attention_static",
-            "oscar_decode_step", "oscar_multiquery_attention")
+            "oscar_decode_step", "oscar_multiquery_attention",
+            "oscar_calibration_workspace_size", "oscar_query_covariance_device",
+            "oscar_score_covariance_device", "oscar_clip_threshold_device")
 
 
 class OscarError(RuntimeError):
@@ -73,6 +75,11 @@ def lib() -> ctypes.CDLL:
             "oscar_decode_attention_static": (I32, [P, P, P, I32, I32, P, P]),
             "oscar_decode_step": (I32, [P, P, P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_multiquery_attention": (I32, [P, P, P, P, I32, I32, I32, P, P, ctypes.c_size_t, P]),
+            "oscar_calibration_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I64]),
+            "oscar_query_covariance_device": (I32, [I32, I32, I32, I64, P, P, P, ctypes.c_size_t, P]),
+            "oscar_score_covariance_device": (I32, [I32, I32, I32, I64, P, P, P, P, P,
+                                                    ctypes.c_size_t, P]),
+            "oscar_clip_threshold_device": (I32, [I32, I32, I64, P, P, D, P, P, ctypes.c_size_t, P]),
             "oscar_status_string": (ctypes.c_char_p, [I32]),
             "oscar_version": (I32, []),
         }
@@ -265,6 +272,42 @@ def oscar_decode_attention_static(cache: Cache, q, seq_lens, max_seq_len: int, o
            lib().oscar_decode_attention_static(ctypes.byref(d), _ptr(q), _ptr(seq_lens),
                                                int(seq_lens.numel()), int(max_seq_len), _ptr(out),
                                                _stream(stream)))
+
+
+def oscar_calibration_workspace_size(num_kv_heads: int, num_q_heads: int, d: int, n: int) -> int:
+    return int(lib().oscar_calibration_workspace_size(num_kv_heads, num_q_heads, d, n))
+
+
+def _ws_bytes(workspace) -> int:
+    return workspace.numel() * workspace.element_size()
+
+
+def oscar_query_covariance_device(q, num_kv_heads: int, c_out, workspace, stream=None):
+    """C_Q per KV head on the device: q bf16 [n][Hq][d] -> c_out fp64 [Hkv][d][d]."""
+    n, hq, d = (int(x) for x in q.shape)
+    _check("oscar_query_covariance_device",
+           lib().oscar_query_covariance_device(num_kv_heads, hq, d, n, _ptr(q), _ptr(c_out),
+                                               _ptr(workspace), _ws_bytes(workspace),
+                                               _stream(stream)))
+
+
+def oscar_score_covariance_device(q, k, v, c_out, workspace, stream=None):
+    """C_S per KV head on the device: q bf16 [n][Hq][d], k/v bf16 [n][Hkv][d]."""
+    n, hq, d = (int(x) for x in q.shape)
+    hkv = int(k.shape[1])
+    _check("oscar_score_covariance_device",
+           lib().oscar_score_covariance_device(hkv, hq, d, n, _ptr(q), _ptr(k), _ptr(v),
+                                               _ptr(c_out), _ptr(workspace), _ws_bytes(workspace),
+                                               _stream(stream)))
+
+
+def oscar_clip_threshold_device(x, r, percentile: float, clip_out, workspace, stream=None):
+    """Clip per KV head on the device: x bf16 [n][Hkv][d], r fp32 [Hkv][d][d]."""
+    n, hkv, d = (int(x_) for x_ in x.shape)
+    _check("oscar_clip_threshold_device",
+           lib().oscar_clip_threshold_device(hkv, d, n, _ptr(x), _ptr(r), float(percentile),
+                                             _ptr(clip_out), _ptr(workspace), _ws_bytes(workspace),
+                                             _stream(stream)))
 
 
 def oscar_device_sm_count() -> int:

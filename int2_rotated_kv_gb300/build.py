@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "liboscar.so")
-SOURCES = ["host_rotation.cpp", "quantize.cu", "decode.cu"]
+SOURCES = ["host_rotation.cpp", "quantize.cu", "decode.cu", "calib.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

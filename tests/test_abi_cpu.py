@@ -140,3 +140,34 @@ def test_argument_errors_before_any_launch(L):
     assert lib.oscar_quantize_append(ctypes.byref(bf_only), 1, 1, 1, 2, None) == -1
     assert lib.oscar_decode_attention_bf16(ctypes.byref(bf_only), 4096, 4096, 1, 16, 4096, 4096, 8,
                                            None) == -3   # reaches the workspace check
+
+
+def test_calibration_argument_errors_before_any_launch(L):
+    lib = L.lib()
+    ws = lambda *a: lib.oscar_calibration_workspace_size(*a)
+    assert ws(8, 32, 128, 8192) > 2 * 8192 * 32 * 128 * 2      # holds the O pair at least
+    assert ws(1, 4, 64, 1) > 0
+    for bad in ((8, 32, 96, 100), (8, 24, 128, 100), (8, 36, 128, 100), (0, 4, 64, 10),
+                (1, 4, 64, 0), (1, 4, 64, (1 << 24) + 1)):
+        assert ws(*bad) == 0, bad
+    big = 1 << 30
+    # shape errors come first, then null / misaligned pointers, then the workspace size
+    assert lib.oscar_query_covariance_device(1, 4, 96, 10, 4096, 4096, 4096, big, None) == -2
+    assert lib.oscar_query_covariance_device(2, 3, 64, 10, 4096, 4096, 4096, big, None) == -1
+    assert lib.oscar_query_covariance_device(1, 4, 64, 10, None, 4096, 4096, big, None) == -1
+    assert lib.oscar_query_covariance_device(1, 4, 64, 10, 4100, 4096, 4096, big, None) == -1
+    assert lib.oscar_query_covariance_device(1, 4, 64, 10, 4096, 4096, 4096, 64, None) == -3
+    assert lib.oscar_score_covariance_device(1, 32, 64, 10, 4096, 4096, 4096, 4096, 4096, big,
+                                             None) == -2                 # G = 32
+    assert lib.oscar_score_covariance_device(1, 4, 64, 10, 4096, None, 4096, 4096, 4096, big,
+                                             None) == -1
+    assert lib.oscar_score_covariance_device(1, 4, 64, 10, 4096, 4096, 4096, 4096, 4096, 64,
+                                             None) == -3
+    assert lib.oscar_clip_threshold_device(1, 64, 10, 4096, 4096, 100.5, 4096, 4096, big,
+                                           None) == -1
+    assert lib.oscar_clip_threshold_device(1, 64, 10, 4096, 4096, float("nan"), 4096, 4096, big,
+                                           None) == -1
+    assert lib.oscar_clip_threshold_device(1, 64, 10, 4096, None, 99.9, 4096, 4096, big,
+                                           None) == -1
+    assert lib.oscar_clip_threshold_device(1, 64, 10, 4096, 4096, 99.9, 4096, 4096, 64,
+                                           None) == -3
