@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--n-calib", type=int, default=None)
     ap.add_argument("--profile", action="store_true",
                     help="minimal run for ncu: one layer cache, eager steps, no extra legs")
+    ap.add_argument("--leg", default=None, choices=sorted(EXTRA_LEGS),
+                    help="run one extra leg alone and print its JSON (for profiling)")
     return ap.parse_args()
 
 
@@ -786,6 +788,17 @@ def extra_budget(dev, l2, n_calib, budget=40e9):
     return res
 
 
+# Extra legs: name -> fn(device, l2_bytes, calibration tokens for the rotations).
+# The calibration leg times calibration itself, on the 8192 tokens of the 8B workload.
+EXTRA_LEGS = {
+    synth.QWEN3_32B_128K.name: extra_long,
+    synth.QWEN3_4B_PREFIX.name: extra_prefix,
+    synth.QWEN3_8B_BUDGET.name: extra_budget,
+    "qwen3_8b_32k_chunk16": extra_multiquery,
+    "qwen3_8b_calibration_8192": lambda dev, l2, _n: extra_calibration(dev, l2, 8192),
+}
+
+
 # --------------------------------------------------------------------- main
 
 def main():
@@ -806,6 +819,10 @@ def main():
             dist.barrier()
     from int2_rotated_kv_gb300 import _lib as L
     L.lib()
+    if args.leg:
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        print(json.dumps({"leg": args.leg, **EXTRA_LEGS[args.leg](dev, l2, 2048)}), flush=True)
+        return
     w = synth.WORKLOADS[args.workload]
     n_calib = args.n_calib or w.n_calib
     t0 = time.time()
@@ -896,10 +913,7 @@ def main():
         ex = {}
         del dec
         torch.cuda.empty_cache()
-        legs = ((synth.QWEN3_32B_128K.name, extra_long), (synth.QWEN3_4B_PREFIX.name, extra_prefix),
-                (synth.QWEN3_8B_BUDGET.name, extra_budget), ("qwen3_8b_32k_chunk16", extra_multiquery),
-                ("qwen3_8b_calibration_8192", extra_calibration))
-        for name, fn in legs:
+        for name, fn in EXTRA_LEGS.items():
             try:
                 ex[name] = fn(dev, l2, 2048)
             except Exception as e:
