@@ -21,6 +21,12 @@
  *     of time) are never trapped: the kernel skips the bad access and ORs a bit
  *     into the optional device word desc->status (see OSCAR_DEVERR_*).
  *   - `stream` is a cudaStream_t passed as void*; 0 means the legacy stream.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the kernel before it on the stream drains, and reads that
+ *     kernel's results only after waiting for it.  The rotations desc->r_k and
+ *     desc->r_v are constants of the layer and are read before that wait, so
+ *     the kernel launched immediately before a call on its stream must not
+ *     write them (any copy or other stream-ordered work in between suffices).
  *   - Calls are stateless and may be issued from several host threads.
  *
  * Cache format (one layer).  Page size 16 tokens, quantisation group 32

@@ -383,10 +383,12 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
       bulk_g2s(wring + i * SB, pool_h + max(wids[kDWarps * i], 0) * pstride, SB, &wbar[i]);
     }
   }
-  // ---- query operand, once the rotated query is complete (warp 0 stages it)
+  // ---- query operand, once the rotated query is complete: warp 0 reads q'
+  // once and stages the MMA operand and the zero-term operand for every warp
   pdl_wait();
-  uint32_t qz = 0;
-  {
+  uint32_t* qzs = reinterpret_cast<uint32_t*>(qbs + NK * 32);
+  if (warp == 0) {
+    uint32_t qz = 0;
     const float* qr = p.qrot + (static_cast<size_t>(b) * p.hq + qh0 + gid) * D;
     float gs[NG];
 #pragma unroll
@@ -395,16 +397,14 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     for (int kk = 0; kk < NK; ++kk) {
       float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
       if (gid < G) {
-        v0 = *reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig);
-        v1 = *reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig + 8);
+        v0 = __ldcg(reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig));
+        v1 = __ldcg(reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig + 8));
       }
       gs[kk >> 1] += (v0.x + v0.y) + (v1.x + v1.y);
-      if (warp == 0) {
-        // codes of k-step parity i and channel half h are read at 4^i * 16^h
-        const float sc = (kk & 1) ? 0.25f : 1.f;
-        qbs[kk * 32 + lane] = make_uint2(pack_half2(v0.x * sc, v0.y * sc),
-                                         pack_half2(v1.x * sc * 0.0625f, v1.y * sc * 0.0625f));
-      }
+      // codes of k-step parity i and channel half h are read at 4^i * 16^h
+      const float sc = (kk & 1) ? 0.25f : 1.f;
+      qbs[kk * 32 + lane] = make_uint2(pack_half2(v0.x * sc, v0.y * sc),
+                                       pack_half2(v1.x * sc * 0.0625f, v1.y * sc * 0.0625f));
     }
     float mine = 0.f;
 #pragma unroll
@@ -420,8 +420,10 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
       qz = static_cast<uint32_t>(__half_as_ushort(hi)) |
            (static_cast<uint32_t>(__half_as_ushort(lo16)) << 16);
     }
+    qzs[lane] = qz;
   }
   __syncthreads();
+  const uint32_t qz = qzs[lane];
   if (lane == 0) {
     if (deferred >= 0) {
       mbar_arrive_expect_tx(&wbar[deferred], SB);

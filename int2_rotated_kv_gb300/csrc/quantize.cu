@@ -366,15 +366,16 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
   const int grp = blockIdx.x % NG, chunk = blockIdx.x / NG;
   const int h = blockIdx.y, kv = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // programmatic stream serialisation: inputs are read only after the
-  // predecessor grid has completed; then the next kernel may launch
-  pdl_wait();
-  pdl_trigger();
+  // The layer's rotation is a constant of the cache and is read while the
+  // predecessor grid may still run; every other input only after it has
+  // completed (programmatic stream serialisation).
   const float* rot = (kv ? p.r_v : p.r_k) + static_cast<size_t>(h) * D * D + 32 * grp;
   for (int e = tid; e < D * 8; e += kQThreads) {       // float4 e%8 of row e/8
     const int i = e >> 3, c4 = e & 7;
     reinterpret_cast<float4*>(&rs[i][0])[c4] = reinterpret_cast<const float4*>(rot + i * D)[c4];
   }
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const float clip = (kv ? p.clip_v : p.clip_k)[h];
   const uint16_t* src = kv ? p.v_src : p.k_src;
