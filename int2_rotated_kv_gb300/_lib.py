@@ -48,6 +48,7 @@ class CacheDesc(ctypes.Structure):
         ("r_k", ctypes.c_void_p), ("r_v", ctypes.c_void_p),
         ("clip_k", ctypes.c_void_p), ("clip_v", ctypes.c_void_p),
         ("status", ctypes.c_void_p),
+        ("code_bits", ctypes.c_int32),
     ]
 
 
@@ -155,9 +156,10 @@ def _stream(stream):
 class Cache:
     """Device tensors of one layer's cache plus its C descriptor.
 
-    int2_pool: uint8 [num_int2_pages * Hkv * 12d]; bf16_pool: bfloat16
-    [num_bf16_pages * Hkv * 32d]; page tables int32 [batch, max_pages_per_seq];
-    r_k, r_v fp32 [Hkv, d, d]; clip_k, clip_v fp32 [Hkv]; status int32 [1].
+    int2_pool: uint8 [num_int2_pages * Hkv * 12d] (INT4 variant, code_bits 4:
+    20d per page-head); bf16_pool: bfloat16 [num_bf16_pages * Hkv * 32d]; page
+    tables int32 [batch, max_pages_per_seq]; r_k, r_v fp32 [Hkv, d, d]; clip_k,
+    clip_v fp32 [Hkv]; status int32 [1].
     """
     num_kv_heads: int
     num_q_heads: int
@@ -173,11 +175,12 @@ class Cache:
     clip_k: object = None
     clip_v: object = None
     status: object = None
+    code_bits: int = 2
 
     def desc(self) -> CacheDesc:
         key = tuple(_ptr(t) for t in (self.int2_pool, self.bf16_pool, self.int2_page_table,
                                       self.bf16_page_table, self.r_k, self.r_v, self.clip_k,
-                                      self.clip_v, self.status))
+                                      self.clip_v, self.status)) + (self.code_bits,)
         cached = self.__dict__.get("_desc")
         if cached is not None and cached[0] == key:
             return cached[1]
@@ -185,11 +188,12 @@ class Cache:
         desc = CacheDesc(
             self.num_kv_heads, self.num_q_heads, d, self.sink, self.window,
             int(self.bf16_page_table.shape[1]),
-            0 if self.int2_pool is None else self.int2_pool.numel() // (self.num_kv_heads * 12 * d),
+            0 if self.int2_pool is None
+            else self.int2_pool.numel() // (self.num_kv_heads * (4 * self.code_bits + 4) * d),
             self.bf16_pool.numel() // (self.num_kv_heads * 32 * d),
             _ptr(self.int2_pool), _ptr(self.bf16_pool), _ptr(self.int2_page_table),
             _ptr(self.bf16_page_table), _ptr(self.r_k), _ptr(self.r_v), _ptr(self.clip_k),
-            _ptr(self.clip_v), _ptr(self.status))
+            _ptr(self.clip_v), _ptr(self.status), self.code_bits)
         self.__dict__["_desc"] = (key, desc)
         return desc
 

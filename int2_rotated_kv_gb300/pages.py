@@ -86,8 +86,10 @@ def plan(seq_lens, sink: int, window: int, *, shared_prefix_tokens: int = 0,
     return PagePlan(it, bt, max(n2, 1), max(nb, 1), maxp)
 
 
-def int2_bytes_per_page(hkv: int, d: int) -> int:
-    return hkv * 12 * d
+def int2_bytes_per_page(hkv: int, d: int, code_bits: int = 2) -> int:
+    """Code-pool bytes of one page: 12d per KV head for INT2, 20d for the INT4
+    variant (two 2-bit planes)."""
+    return hkv * (4 * code_bits + 4) * d
 
 
 def bf16_bytes_per_page(hkv: int, d: int) -> int:
@@ -95,13 +97,16 @@ def bf16_bytes_per_page(hkv: int, d: int) -> int:
 
 
 def allocate(pp: PagePlan, *, hkv: int, hq: int, d: int, sink: int, window: int, device,
-             r_k=None, r_v=None, clip_k=None, clip_v=None, with_status: bool = True):
-    """Device pools (zeroed) and tables for a plan; returns a binding ``Cache``."""
+             r_k=None, r_v=None, clip_k=None, clip_v=None, with_status: bool = True,
+             code_bits: int = 2):
+    """Device pools (zeroed) and tables for a plan; returns a binding ``Cache``.
+    code_bits: 2 (INT2 pages) or 4 (the INT4 variant)."""
     import torch
 
     from ._lib import Cache
     dev = torch.device(device)
-    int2 = torch.zeros(pp.num_int2_pages * int2_bytes_per_page(hkv, d), dtype=torch.uint8, device=dev)
+    int2 = torch.zeros(pp.num_int2_pages * int2_bytes_per_page(hkv, d, code_bits), dtype=torch.uint8,
+                       device=dev)
     bf = torch.zeros(pp.num_bf16_pages * hkv * 32 * d, dtype=torch.bfloat16, device=dev)
 
     def t(x, dt):
@@ -111,4 +116,4 @@ def allocate(pp: PagePlan, *, hkv: int, hq: int, d: int, sink: int, window: int,
                  t(pp.int2_table, torch.int32), t(pp.bf16_table, torch.int32),
                  t(r_k, torch.float32), t(r_v, torch.float32), t(clip_k, torch.float32),
                  t(clip_v, torch.float32),
-                 torch.zeros(1, dtype=torch.int32, device=dev) if with_status else None)
+                 torch.zeros(1, dtype=torch.int32, device=dev) if with_status else None, code_bits)

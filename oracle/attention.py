@@ -56,36 +56,37 @@ def softmax_attention_loops(q, k, v, scale=None):
     return np.array(out)
 
 
-def reconstruct(x: np.ndarray, r: np.ndarray, clip: float) -> np.ndarray:
-    """Stored INT2 form of tokens x [n, d], mapped back to the original basis:
-    dequantise(quantise(x R)) R^T."""
-    codes, s, z = quant.quantize(quant.rotate(x, r), clip)
+def reconstruct(x: np.ndarray, r: np.ndarray, clip: float,
+                levels: int = quant.INT2_MAX_CODE) -> np.ndarray:
+    """Stored INT2 (or INT4: levels 15) form of tokens x [n, d], mapped back to
+    the original basis: dequantise(quantise(x R)) R^T."""
+    codes, s, z = quant.quantize(quant.rotate(x, r), clip, levels=levels)
     return quant.dequantize(codes, s, z) @ np.asarray(r, np.float64).T
 
 
 def effective_kv(k: np.ndarray, v: np.ndarray, L: int, sink: int, window: int,
-                 rk, rv, ck: float, cv: float):
+                 rk, rv, ck: float, cv: float, levels: int = quant.INT2_MAX_CODE):
     """Keys/values as the cache holds them for a sequence of length L."""
     k = np.asarray(k[:L], np.float64).copy()
     v = np.asarray(v[:L], np.float64).copy()
     m = cache.is_int2(np.arange(L), L, sink, window)
     if m.any():
-        k[m] = reconstruct(k[m], rk, ck)
-        v[m] = reconstruct(v[m], rv, cv)
+        k[m] = reconstruct(k[m], rk, ck, levels)
+        v[m] = reconstruct(v[m], rv, cv, levels)
     return k, v
 
 
 def mixed_decode(q: np.ndarray, k: list, v: list, lens, rot: "cache.Rotations", *,
-                 sink: int, window: int, gqa: int) -> np.ndarray:
+                 sink: int, window: int, gqa: int, levels: int = quant.INT2_MAX_CODE) -> np.ndarray:
     """out [B, Hq, d] for decode queries q [B, Hq, d]; query head hq reads KV
-    head hq // gqa; k[b][h], v[b][h] are [L_b, d]."""
+    head hq // gqa; k[b][h], v[b][h] are [L_b, d].  levels 15: the INT4 variant."""
     B, Hq, d = q.shape
     out = np.zeros((B, Hq, d))
     for b in range(B):
         L = int(lens[b])
         for h in range(Hq // gqa):
             ke, ve = effective_kv(k[b][h], v[b][h], L, sink, window,
-                                  rot.rk[h], rot.rv[h], rot.ck[h], rot.cv[h])
+                                  rot.rk[h], rot.rv[h], rot.ck[h], rot.cv[h], levels)
             out[b, h * gqa:(h + 1) * gqa] = softmax_attention(q[b, h * gqa:(h + 1) * gqa], ke, ve)
     return out
 

@@ -50,23 +50,26 @@ class ExpectedPools:
 def expected_pools(k, v, lens, rot: Rotations, *, sink: int, window: int, d: int, hkv: int,
                    int2_table: np.ndarray, bf16_table: np.ndarray,
                    num_int2_pages: int, num_bf16_pages: int, kappa: float | None = None,
-                   tokens=None) -> ExpectedPools:
+                   tokens=None, bits: int = 2) -> ExpectedPools:
     """Pools after every token of every sequence has been placed.
 
     k[b][h], v[b][h]: float arrays [L_b, d] of bf16 values.  ``tokens`` (optional)
     restricts to a dict {b: iterable of positions}; by default all positions.
     ``kappa`` enables near-boundary flags for kernels with fp32 rotation error.
+    ``bits``: 2 (INT2 pages) or 4 (the INT4 variant: codes 0..15 in two planes).
     """
-    blk = layout.int2_block_bytes(d)
+    levels = quant.INT2_MAX_CODE if bits == 2 else quant.INT4_MAX_CODE
+    blk = layout.int2_block_bytes(d, bits)
     bblk = layout.bf16_block_bytes(d) // 2
     int2 = np.zeros(num_int2_pages * hkv * blk, np.uint8)
     idef = np.zeros_like(int2, dtype=bool)
     imay = np.zeros_like(int2, dtype=bool)
     bf = np.zeros(num_bf16_pages * hkv * bblk, np.uint16)
     bdef = np.zeros_like(bf, dtype=bool)
-    tb = layout.tables(d)
+    tb = layout.tables(d, bits)
     owner, bowner = tb["owner"], tb["bowner"]
-    o = layout.offsets(d)
+    o = layout.offsets(d, bits)
+    plane_offs = [o["plane"] * q for q in range(layout.planes(bits))]
     ng = d // quant.GROUP
     nfe = nfg = 0
     for b, L in enumerate(lens):
@@ -80,11 +83,13 @@ def expected_pools(k, v, lens, rot: Rotations, *, sink: int, window: int, d: int
             vv = np.asarray(v[b][h], np.float64)
             ti = pos[m_int2]
             if ti.size:
-                kc, ks, kz = quant.quantize(quant.rotate(kk[ti], rot.rk[h]), rot.ck[h])
-                vc, vs, vz = quant.quantize(quant.rotate(vv[ti], rot.rv[h]), rot.cv[h])
+                kc, ks, kz = quant.quantize(quant.rotate(kk[ti], rot.rk[h]), rot.ck[h], levels=levels)
+                vc, vs, vz = quant.quantize(quant.rotate(vv[ti], rot.rv[h]), rot.cv[h], levels=levels)
                 if kappa is not None:
-                    ekf, gkf = quant.near_boundary_flags(kk[ti], rot.rk[h], rot.ck[h], kappa)
-                    evf, gvf = quant.near_boundary_flags(vv[ti], rot.rv[h], rot.cv[h], kappa)
+                    ekf, gkf = quant.near_boundary_flags(kk[ti], rot.rk[h], rot.ck[h], kappa,
+                                                         levels=levels)
+                    evf, gvf = quant.near_boundary_flags(vv[ti], rot.rv[h], rot.cv[h], kappa,
+                                                         levels=levels)
                     nfe += int(ekf.sum() + evf.sum())
                     nfg += int(gkf.sum() + gvf.sum())
                 for n, t in enumerate(ti):
@@ -92,25 +97,30 @@ def expected_pools(k, v, lens, rot: Rotations, *, sink: int, window: int, d: int
                     base = (page * hkv + h) * blk
                     block = int2[base:base + blk]
                     slot = int(t % PAGE)
-                    layout.pack_int2_block(block, d, slot, kc[n], ks[n], kz[n], vc[n], vs[n], vz[n])
+                    layout.pack_int2_block(block, d, slot, kc[n], ks[n], kz[n], vc[n], vs[n], vz[n],
+                                           bits=bits)
                     idef[base:base + blk] |= owner == slot
                     if kappa is not None:
                         may = imay[base:base + blk]
-                        kbytes = o["Kc"] + tb["kbyte"][slot]
-                        vbytes = o["Vc"] + tb["vbyte"][slot]
+                        for po in plane_offs:
+                            kbytes = o["Kc"] + po + tb["kbyte"][slot]
+                            vbytes = o["Vc"] + po + tb["vbyte"][slot]
+                            for g in range(ng):
+                                cols = slice(32 * g, 32 * g + 32)
+                                if gkf[n, g]:
+                                    may[kbytes[cols]] = True
+                                if gvf[n, g]:
+                                    may[vbytes[cols]] = True
+                            may[kbytes[ekf[n]]] = True
+                            may[vbytes[evf[n]]] = True
                         for g in range(ng):
-                            cols = slice(32 * g, 32 * g + 32)
                             if gkf[n, g]:
-                                may[kbytes[cols]] = True
                                 e0 = o["Ksz"] + 4 * (slot * ng + g)
                                 may[e0:e0 + 4] = True
                             if gvf[n, g]:
-                                may[vbytes[cols]] = True
                                 for part in ("Vs", "Vz"):
                                     e0 = o[part] + 2 * tb["vsz"][slot, g]
                                     may[e0:e0 + 2] = True
-                        may[kbytes[ekf[n]]] = True
-                        may[vbytes[evf[n]]] = True
             tb16 = pos[~m_int2]
             for t in tb16:
                 page = int(bf16_table[b, t // PAGE])

@@ -29,6 +29,14 @@ as 32-bit words of two bf16 (first element in the low half):
   element index = 2*word + e.
 
 Pools: block (physical page p, KV head h) sits at (p*Hkv + h) * block_bytes.
+
+INT4 variant (bits = 4): a 4-bit code c is stored as two 2-bit planes, the high
+bits c >> 2 in plane 0 and the low bits c & 3 in plane 1, each plane laid out
+exactly as the INT2 code area above.  Block (20*d bytes):
+  Kc plane 0 [0, 4d) | Kc plane 1 [4d, 8d) | Ksz [8d, 10d) | Vc plane 0 [10d, 14d)
+  | Vc plane 1 [14d, 18d) | Vs [18d, 19d) | Vz [19d, 20d).
+In general with P = bits/2 planes: Kc plane q at 4d*q, Ksz at 4dP, Vc plane q
+at 4dP + 2d + 4d*q, Vs at 8dP + 2d, Vz at 8dP + 3d; block (8P + 4)*d bytes.
 """
 from __future__ import annotations
 
@@ -38,16 +46,26 @@ PAGE = 16
 GROUP = 32
 
 
-def int2_block_bytes(d: int) -> int:
-    return 12 * d
+def planes(bits: int) -> int:
+    if bits not in (2, 4):
+        raise ValueError("code bits must be 2 or 4")
+    return bits // 2
+
+
+def int2_block_bytes(d: int, bits: int = 2) -> int:
+    """Bytes of one code page-head block (INT2: 12d, INT4: 20d)."""
+    return (8 * planes(bits) + 4) * d
 
 
 def bf16_block_bytes(d: int) -> int:
     return 64 * d
 
 
-def offsets(d: int) -> dict:
-    return {"Kc": 0, "Ksz": 4 * d, "Vc": 6 * d, "Vs": 10 * d, "Vz": 11 * d}
+def offsets(d: int, bits: int = 2) -> dict:
+    """Byte offsets of the block's parts; Kc / Vc are plane 0, plane q adds 4d*q."""
+    P = planes(bits)
+    return {"Kc": 0, "Ksz": 4 * d * P, "Vc": 4 * d * P + 2 * d, "Vs": 8 * d * P + 2 * d,
+            "Vz": 8 * d * P + 3 * d, "plane": 4 * d}
 
 
 def k_code_pos(t: int, j: int, d: int):
@@ -97,9 +115,9 @@ def bf16_v_elem(t: int, j: int) -> int:
 _TABLES: dict = {}
 
 
-def tables(d: int) -> dict:
-    if d in _TABLES:
-        return _TABLES[d]
+def tables(d: int, bits: int = 2) -> dict:
+    if (d, bits) in _TABLES:
+        return _TABLES[(d, bits)]
     ng = d // GROUP
     kbyte = np.zeros((PAGE, d), np.int64)
     kbit = np.zeros((PAGE, d), np.int64)
@@ -117,11 +135,12 @@ def tables(d: int) -> dict:
     for t in range(PAGE):
         for g in range(ng):
             vsz[t, g] = vsz_index(t, g, d)
-    o = offsets(d)
-    # owner token of every byte of an INT2 block (each byte belongs to one token)
-    owner = np.full(int2_block_bytes(d), -1, np.int64)
-    owner[o["Kc"] + kbyte] = np.repeat(np.arange(PAGE), d).reshape(PAGE, d)
-    owner[o["Vc"] + vbyte] = np.repeat(np.arange(PAGE), d).reshape(PAGE, d)
+    o = offsets(d, bits)
+    # owner token of every byte of a code block (each byte belongs to one token)
+    owner = np.full(int2_block_bytes(d, bits), -1, np.int64)
+    for q in range(planes(bits)):
+        owner[o["Kc"] + o["plane"] * q + kbyte] = np.repeat(np.arange(PAGE), d).reshape(PAGE, d)
+        owner[o["Vc"] + o["plane"] * q + vbyte] = np.repeat(np.arange(PAGE), d).reshape(PAGE, d)
     for t in range(PAGE):
         for g in range(ng):
             base = o["Ksz"] + 4 * (t * ng + g)
@@ -134,24 +153,31 @@ def tables(d: int) -> dict:
     bowner[16 * d + bv] = np.repeat(np.arange(PAGE), d).reshape(PAGE, d)
     tb = dict(kbyte=kbyte, kbit=kbit, vbyte=vbyte, vbit=vbit, bk=bk, bv=bv, vsz=vsz,
               owner=owner, bowner=bowner)
-    _TABLES[d] = tb
+    _TABLES[(d, bits)] = tb
     return tb
 
 
-def pack_int2_block(block: np.ndarray, d: int, t: int, kc, ks, kz, vc, vs, vz) -> None:
-    """Write token t's codes/scales/zeros into an INT2 block (uint8 [12d], in place).
+def pack_int2_block(block: np.ndarray, d: int, t: int, kc, ks, kz, vc, vs, vz,
+                    bits: int = 2) -> None:
+    """Write token t's codes/scales/zeros into a code block (uint8, in place;
+    12d bytes for INT2, 20d for INT4).
 
-    kc, vc: uint8 [d] codes; ks, kz, vs, vz: float16 [ng]."""
-    tb = tables(d)
-    o = offsets(d)
+    kc, vc: uint8 [d] codes (0..3 or 0..15); ks, kz, vs, vz: float16 [ng]."""
+    tb = tables(d, bits)
+    o = offsets(d, bits)
     ng = d // GROUP
-    kb = o["Kc"] + tb["kbyte"][t]
-    vb = o["Vc"] + tb["vbyte"][t]
-    # clear this token's code bytes, then OR the fields in
-    block[kb] = 0
-    block[vb] = 0
-    np.bitwise_or.at(block, kb, (np.asarray(kc, np.uint8) << tb["kbit"][t]).astype(np.uint8))
-    np.bitwise_or.at(block, vb, (np.asarray(vc, np.uint8) << tb["vbit"][t]).astype(np.uint8))
+    P = planes(bits)
+    kc = np.asarray(kc, np.uint8)
+    vc = np.asarray(vc, np.uint8)
+    for q in range(P):
+        shift = 2 * (P - 1 - q)          # plane 0 holds the highest two bits
+        kb = o["Kc"] + o["plane"] * q + tb["kbyte"][t]
+        vb = o["Vc"] + o["plane"] * q + tb["vbyte"][t]
+        # clear this token's code bytes, then OR the fields in
+        block[kb] = 0
+        block[vb] = 0
+        np.bitwise_or.at(block, kb, (((kc >> shift) & 3) << tb["kbit"][t]).astype(np.uint8))
+        np.bitwise_or.at(block, vb, (((vc >> shift) & 3) << tb["vbit"][t]).astype(np.uint8))
     ksz = np.zeros(ng * 2, np.float16)
     ksz[0::2] = ks
     ksz[1::2] = kz
@@ -162,13 +188,18 @@ def pack_int2_block(block: np.ndarray, d: int, t: int, kc, ks, kz, vc, vs, vz) -
     vz_view[tb["vsz"][t]] = vz
 
 
-def unpack_int2_block(block: np.ndarray, d: int):
+def unpack_int2_block(block: np.ndarray, d: int, bits: int = 2):
     """Inverse of ``pack_int2_block`` for all 16 slots: (kc, ks, kz, vc, vs, vz)."""
-    tb = tables(d)
-    o = offsets(d)
+    tb = tables(d, bits)
+    o = offsets(d, bits)
     ng = d // GROUP
-    kc = (block[o["Kc"] + tb["kbyte"]] >> tb["kbit"]) & 3
-    vc = (block[o["Vc"] + tb["vbyte"]] >> tb["vbit"]) & 3
+    P = planes(bits)
+    kc = np.zeros((PAGE, d), np.int64)
+    vc = np.zeros((PAGE, d), np.int64)
+    for q in range(P):
+        shift = 2 * (P - 1 - q)
+        kc |= ((block[o["Kc"] + o["plane"] * q + tb["kbyte"]] >> tb["kbit"]) & 3).astype(np.int64) << shift
+        vc |= ((block[o["Vc"] + o["plane"] * q + tb["vbyte"]] >> tb["vbit"]) & 3).astype(np.int64) << shift
     ksz = block[o["Ksz"]:o["Vc"]].view(np.float16).reshape(PAGE, ng, 2)
     vs_view = block[o["Vs"]:o["Vz"]].view(np.float16)
     vz_view = block[o["Vz"]:o["Vz"] + d].view(np.float16)

@@ -18,13 +18,18 @@ precision of the library's kernels, step by step:
     s16  = fp16( fp32( fp32(mx - mn) / 3 ) ),   z16 = fp16(mn)
     code = 0 if s16 == 0 else clamp(rint( fp32( fp32(yc - z16) / s16 ) ), 0, 3)
 Dequantisation is y_hat = code * s16 + z16.
+
+INT4 variant (a format variant beside the pages' INT2, for the comparison the
+pages draw with INT4 caches in [Summary 4]): the same steps with 16 levels, i.e.
+the divisor 3 and the top code 3 become 15 (``levels`` = largest code).
 """
 from __future__ import annotations
 
 import numpy as np
 
 GROUP = 32
-LEVELS = 4
+INT2_MAX_CODE = 3     # 4 levels
+INT4_MAX_CODE = 15    # 16 levels
 
 
 def rotate(x: np.ndarray, r: np.ndarray) -> np.ndarray:
@@ -32,9 +37,9 @@ def rotate(x: np.ndarray, r: np.ndarray) -> np.ndarray:
     return np.asarray(x, np.float64) @ np.asarray(r, np.float64)
 
 
-def quantize(y: np.ndarray, clip: float, group: int = GROUP):
-    """Quantise rotated vectors y [..., d].  Returns (codes uint8 [..., d],
-    s16 float16 [..., d/group], z16 float16 [..., d/group])."""
+def quantize(y: np.ndarray, clip: float, group: int = GROUP, levels: int = INT2_MAX_CODE):
+    """Quantise rotated vectors y [..., d] to codes 0..levels.  Returns (codes
+    uint8 [..., d], s16 float16 [..., d/group], z16 float16 [..., d/group])."""
     y32 = np.asarray(y).astype(np.float32)
     c = np.float32(clip)
     yc = np.minimum(np.maximum(y32, -c), c)
@@ -44,13 +49,13 @@ def quantize(y: np.ndarray, clip: float, group: int = GROUP):
     g = yc.reshape(shp[:-1] + (ng, group))
     mn = g.min(axis=-1)
     mx = g.max(axis=-1)
-    s32 = np.float32(mx - mn) / np.float32(3.0)
+    s32 = np.float32(mx - mn) / np.float32(levels)
     s16 = s32.astype(np.float32).astype(np.float16)
     z16 = mn.astype(np.float16)
     with np.errstate(divide="ignore", invalid="ignore"):
         num = (g - z16.astype(np.float32)[..., None]).astype(np.float32)
         t = (num / s16.astype(np.float32)[..., None]).astype(np.float32)
-        code = np.clip(np.rint(t), 0, LEVELS - 1)
+        code = np.clip(np.rint(t), 0, levels)
     code = np.where((s16 == 0)[..., None], 0, code)
     return code.reshape(shp).astype(np.uint8), s16, z16
 
@@ -72,7 +77,7 @@ def clipped(y: np.ndarray, clip: float) -> np.ndarray:
 
 
 def near_boundary_flags(x: np.ndarray, r: np.ndarray, clip: float, kappa: float,
-                        group: int = GROUP):
+                        group: int = GROUP, levels: int = INT2_MAX_CODE):
     """Entries whose decision may legitimately differ from a kernel whose fp32
     rotated value y' satisfies |y' - y| <= kappa * sum_i |x_i| |R_ij|.
 
@@ -88,7 +93,7 @@ def near_boundary_flags(x: np.ndarray, r: np.ndarray, clip: float, kappa: float,
     elem = np.abs(np.abs(y) - c) <= eps
     # an entry clipped with margin is exactly +-c on both sides
     eps_c = np.where(np.abs(y) - c > eps, 0.0, eps)
-    codes, s16, z16 = quantize(y, clip, group)
+    codes, s16, z16 = quantize(y, clip, group, levels)
     yc = clipped(y, clip).astype(np.float64)
     shp = y.shape
     ng = shp[-1] // group
@@ -100,9 +105,9 @@ def near_boundary_flags(x: np.ndarray, r: np.ndarray, clip: float, kappa: float,
     mx_lo, mx_hi = (gy - ge).max(-1), (gy + ge).max(-1)
     # z16 = fp16(mn): flag if the fp16 rounding can change inside the interval
     gflag = mn_lo.astype(np.float16) != mn_hi.astype(np.float16)
-    # s16 = fp16(fp32(fp32(mx - mn)/3)): the two fp32 steps add a few ulps
-    s_lo = np.maximum((mx_lo - mn_hi) / 3.0 * (1 - 2.0 ** -21), 0.0)
-    s_hi = (mx_hi - mn_lo) / 3.0 * (1 + 2.0 ** -21)
+    # s16 = fp16(fp32(fp32(mx - mn)/levels)): the two fp32 steps add a few ulps
+    s_lo = np.maximum((mx_lo - mn_hi) / levels * (1 - 2.0 ** -21), 0.0)
+    s_hi = (mx_hi - mn_lo) / levels * (1 + 2.0 ** -21)
     gflag |= s_lo.astype(np.float16) != s_hi.astype(np.float16)
     # code: t = (yc - z16)/s16 near a half-integer
     s = s16.astype(np.float64)

@@ -40,14 +40,15 @@ def oracle_rotations(inst, variant=0, n_calib=None):
 
 
 def make_cache(inst, rot, *, window, sink=4, growth=0, shared=0, permute=None, lens=None,
-               max_len=None):
+               max_len=None, bits=2):
     w = inst.workload
     lens = inst.seq_lens if lens is None else lens
     pp = pages.plan(lens, sink, window, shared_prefix_tokens=shared, growth=growth,
                     permute_seed=permute, max_len=max_len)
     c = pages.allocate(pp, hkv=w.num_kv_heads, hq=w.num_q_heads, d=w.head_dim, sink=sink,
                        window=window, device=DEV, r_k=np.stack(rot.rk), r_v=np.stack(rot.rv),
-                       clip_k=np.array(rot.ck, np.float32), clip_v=np.array(rot.cv, np.float32))
+                       clip_k=np.array(rot.ck, np.float32), clip_v=np.array(rot.cv, np.float32),
+                       code_bits=bits)
     return c, pp
 
 
@@ -79,13 +80,13 @@ def pools(cache):
     return cache.int2_pool.cpu().numpy(), cache.bf16_pool.view(t.int16).cpu().numpy().view(np.uint16)
 
 
-def expected(inst, rot, pp, *, window, sink=4, lens=None, kappa=None):
+def expected(inst, rot, pp, *, window, sink=4, lens=None, kappa=None, bits=2):
     w = inst.workload
     lens = inst.seq_lens if lens is None else lens
     return ocache.expected_pools(inst.k, inst.v, lens, rot, sink=sink, window=window,
                                  d=w.head_dim, hkv=w.num_kv_heads, int2_table=pp.int2_table,
                                  bf16_table=pp.bf16_table, num_int2_pages=pp.num_int2_pages,
-                                 num_bf16_pages=pp.num_bf16_pages, kappa=kappa)
+                                 num_bf16_pages=pp.num_bf16_pages, kappa=kappa, bits=bits)
 
 
 def compare_pools(cache, exp):
@@ -124,11 +125,13 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=Non
     Separates the decode kernels' parity from the quantiser's (whose flagged
     near-boundary codes may differ from the oracle's by one step).  ``drop``:
     optional {sequence: logical pages} whose tokens are left out.  ``upto``:
-    optional last visible position per sequence (a query row of a chunk)."""
+    optional last visible position per sequence (a query row of a chunk).  The
+    code width (INT2 or the INT4 variant) is the cache's ``code_bits``."""
     got2, gotb = pools(cache)
     B, Hq, d = q.shape
     hkv = Hq // gqa
-    blk2 = layout.int2_block_bytes(d)
+    bits = getattr(cache, "code_bits", 2)
+    blk2 = layout.int2_block_bytes(d, bits)
     blkb = layout.bf16_block_bytes(d) // 2
     out = np.zeros((B, Hq, d))
     for b in range(B):
@@ -145,7 +148,7 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=Non
                 if mi.any():
                     pid = int(pp.int2_table[b, pg])
                     kc, ks, kz, vc, vs, vz = layout.unpack_int2_block(
-                        got2[(pid * hkv + h) * blk2:(pid * hkv + h + 1) * blk2], d)
+                        got2[(pid * hkv + h) * blk2:(pid * hkv + h + 1) * blk2], d, bits)
                     sl = slots[mi]
                     yk = quant.dequantize(kc[sl], ks[sl], kz[sl])
                     yv = quant.dequantize(vc[sl], vs[sl], vz[sl])

@@ -70,3 +70,28 @@ def test_attention_from_pools_upto_matches_multiquery_oracle():
         got = H.attention_from_pools(cache, pp, q[:, m], lens, rot, sink=4, window=64, gqa=4,
                                      upto=pos[:, m])
         np.testing.assert_allclose(got, ref[:, m], rtol=1e-12, atol=1e-12)
+
+
+def test_attention_from_pools_reads_int4_pools():
+    """The INT4 variant: oracle-packed two-plane pools read back and attended
+    give exactly the oracle's attention with sixteen-level codes."""
+    import torch
+    wl = synth.TINY
+    lens = np.array([300, 90])
+    inst = synth.draw_instance(wl, n_calib=256, seq_lens=lens)
+    rot = attention.calibrate(inst.calib_q, inst.calib_k, inst.calib_v, 0)
+    pp = pages.plan(lens, 4, 64, permute_seed=2)
+    exp = ocache.expected_pools(inst.k, inst.v, lens, rot, sink=4, window=64, d=wl.head_dim,
+                                hkv=1, int2_table=pp.int2_table, bf16_table=pp.bf16_table,
+                                num_int2_pages=pp.num_int2_pages, num_bf16_pages=pp.num_bf16_pages,
+                                bits=4)
+    cache = types.SimpleNamespace(int2_pool=torch.from_numpy(exp.int2.copy()), code_bits=4,
+                                  bf16_pool=torch.from_numpy(exp.bf16.view(np.int16).copy()).view(torch.bfloat16))
+    got = H.attention_from_pools(cache, pp, inst.q, lens, rot, sink=4, window=64, gqa=4)
+    ref = attention.mixed_decode(inst.q, inst.k, inst.v, lens, rot, sink=4, window=64, gqa=4,
+                                 levels=15)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # and sixteen levels sit closer to all-BF16 attention than four do
+    bf = attention.bf16_decode(inst.q, inst.k, inst.v, lens, gqa=4)
+    int2 = attention.mixed_decode(inst.q, inst.k, inst.v, lens, rot, sink=4, window=64, gqa=4)
+    assert attention.rel_l2(ref, bf) < attention.rel_l2(int2, bf)

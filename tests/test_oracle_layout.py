@@ -129,3 +129,61 @@ def test_bf16_words_give_mma_fragments(d):
                 (r0, c0), (r1, c1) = frag_a(lane, reg)
                 assert wk & 0xFFFF == kb[r0, 16 * step + c0] and wk >> 16 == kb[r1, 16 * step + c1]
                 assert wv & 0xFFFF == vb[c0, 16 * step + r0] and wv >> 16 == vb[c1, 16 * step + r1]
+
+
+# ------------------------------------------------------------ INT4 variant (two planes)
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_int4_block_sizes_and_ownership(d):
+    assert layout.int2_block_bytes(d, 4) == 20 * d and layout.int2_block_bytes(d) == 12 * d
+    o = layout.offsets(d, 4)
+    assert (o["Kc"], o["Ksz"], o["Vc"], o["Vs"], o["Vz"]) == (0, 8 * d, 10 * d, 18 * d, 19 * d)
+    tb = layout.tables(d, 4)
+    assert tb["owner"].size == 20 * d and np.all(tb["owner"] >= 0)
+    with pytest.raises(ValueError):
+        layout.planes(3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_int4_pack_unpack_roundtrip(d):
+    rng = np.random.default_rng(5)
+    ng = d // 32
+    blk = np.zeros(layout.int2_block_bytes(d, 4), np.uint8)
+    kc = rng.integers(0, 16, (16, d)).astype(np.uint8)
+    vc = rng.integers(0, 16, (16, d)).astype(np.uint8)
+    ks, kz, vs, vz = (rng.standard_normal((16, ng)).astype(np.float16) for _ in range(4))
+    for t in rng.permutation(16):
+        layout.pack_int2_block(blk, d, t, kc[t], ks[t], kz[t], vc[t], vs[t], vz[t], bits=4)
+    out = layout.unpack_int2_block(blk, d, bits=4)
+    for a, b in zip(out, (kc, ks, kz, vc, vs, vz)):
+        np.testing.assert_array_equal(a, b)
+    layout.pack_int2_block(blk, d, 9, 15 - kc[9], ks[9], kz[9], 15 - vc[9], vs[9], vz[9], bits=4)
+    out2 = layout.unpack_int2_block(blk, d, bits=4)
+    np.testing.assert_array_equal(out2[3][9], 15 - vc[9])
+    np.testing.assert_array_equal(np.delete(out2[3], 9, 0), np.delete(vc, 9, 0))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_int4_planes_are_int2_code_areas(d):
+    """Plane 0 of an INT4 block is the INT2 code area of the high bits c >> 2,
+    plane 1 that of the low bits c & 3 (so each plane keeps the INT2 fragment
+    order pinned above); scales and zeros are the INT2 ones, moved by 8d."""
+    rng = np.random.default_rng(6)
+    ng = d // 32
+    kc = rng.integers(0, 16, (16, d)).astype(np.uint8)
+    vc = rng.integers(0, 16, (16, d)).astype(np.uint8)
+    ks, kz, vs, vz = (rng.standard_normal((16, ng)).astype(np.float16) for _ in range(4))
+    b4 = np.zeros(layout.int2_block_bytes(d, 4), np.uint8)
+    hi = np.zeros(layout.int2_block_bytes(d), np.uint8)
+    lo = np.zeros(layout.int2_block_bytes(d), np.uint8)
+    for t in range(16):
+        layout.pack_int2_block(b4, d, t, kc[t], ks[t], kz[t], vc[t], vs[t], vz[t], bits=4)
+        layout.pack_int2_block(hi, d, t, kc[t] >> 2, ks[t], kz[t], vc[t] >> 2, vs[t], vz[t])
+        layout.pack_int2_block(lo, d, t, kc[t] & 3, ks[t], kz[t], vc[t] & 3, vs[t], vz[t])
+    o2, o4 = layout.offsets(d), layout.offsets(d, 4)
+    np.testing.assert_array_equal(b4[0:4 * d], hi[0:4 * d])
+    np.testing.assert_array_equal(b4[4 * d:8 * d], lo[0:4 * d])
+    np.testing.assert_array_equal(b4[o4["Vc"]:o4["Vc"] + 4 * d], hi[o2["Vc"]:o2["Vc"] + 4 * d])
+    np.testing.assert_array_equal(b4[o4["Vc"] + 4 * d:o4["Vc"] + 8 * d], lo[o2["Vc"]:o2["Vc"] + 4 * d])
+    np.testing.assert_array_equal(b4[o4["Ksz"]:o4["Ksz"] + 2 * d], hi[o2["Ksz"]:o2["Ksz"] + 2 * d])
+    np.testing.assert_array_equal(b4[o4["Vs"]:], hi[o2["Vs"]:])

@@ -99,3 +99,56 @@ def test_identity_and_signed_permutation_rotations_are_exact(d):
     r[np.arange(d), perm] = rng.choice([-1.0, 1.0], d)
     y = quant.rotate(x, r)
     np.testing.assert_array_equal(y[:, perm], x * r[np.arange(d), perm][None, :])
+
+
+# ------------------------------------------------------------ INT4 variant (levels 15)
+
+def test_int4_grid_values_are_their_own_codes():
+    """A group spanning [0, 15] with fp16-exact entries has s16 = 1 and z16 = 0,
+    so every integer entry is its own code and half-integers round to even."""
+    vals = np.concatenate([np.arange(16.0), np.arange(16.0)[::-1]])
+    vals[5], vals[6], vals[7], vals[20] = 0.5, 1.5, 2.5, 14.5
+    codes, s16, z16 = quant.quantize(vals[None, :], 100.0, levels=quant.INT4_MAX_CODE)
+    assert float(s16[0, 0]) == 1.0 and float(z16[0, 0]) == 0.0
+    want = np.rint(vals).astype(np.uint8)      # numpy rint is round-half-even
+    np.testing.assert_array_equal(codes[0], want)
+    assert list(codes[0, [5, 6, 7, 20]]) == [0, 2, 2, 14]
+
+
+def test_int4_range_scale_and_reconstruction_bound():
+    rng = np.random.default_rng(11)
+    y = rng.standard_normal((400, 128)) * np.exp(rng.standard_normal(128))
+    clip = 3.0
+    codes, s16, z16 = quant.quantize(y, clip, levels=15)
+    assert codes.max() <= 15 and codes.min() >= 0 and codes.max() > 3
+    g = quant.clipped(y, clip).reshape(400, 4, 32)
+    np.testing.assert_array_equal(s16, ((g.max(-1) - g.min(-1)) / np.float32(15)).astype(np.float16))
+    yh = quant.dequantize(codes, s16, z16)
+    s = np.repeat(s16.astype(np.float64), 32, axis=-1)
+    z = np.repeat(z16.astype(np.float64), 32, axis=-1)
+    err = np.abs(quant.clipped(y, clip) - yh)
+    bound = s / 2 + 2.0 ** -11 * (np.abs(z) + 15 * s) + 1e-12
+    assert np.all(err <= bound)
+    # sixteen levels: the worst error is about a fifth of the four-level one
+    c2, s2, z2 = quant.quantize(y, clip)
+    e2 = np.abs(quant.clipped(y, clip) - quant.dequantize(c2, s2, z2))
+    assert err.max() < 0.3 * e2.max()
+
+
+def test_int4_flags_cover_only_near_boundary_entries():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((64, 64)).astype(np.float32)
+    r = np.linalg.qr(rng.standard_normal((64, 64)))[0].astype(np.float32)
+    elem, grp = quant.near_boundary_flags(x, r, 2.0, kappa=2.0 ** -16, levels=15)
+    y = quant.rotate(x, r)
+    eps = 2.0 ** -16 * (np.abs(x.astype(np.float64)) @ np.abs(r.astype(np.float64)))
+    for seed in range(3):
+        pert = y + eps * np.random.default_rng(seed).uniform(-1, 1, y.shape)
+        c0, s0, z0 = quant.quantize(y, 2.0, levels=15)
+        c1, s1, z1 = quant.quantize(pert, 2.0, levels=15)
+        ok = ~(elem | np.repeat(grp, 32, axis=-1))
+        assert np.all(c0[ok] == c1[ok])
+        assert np.all(np.abs(c0.astype(int) - c1.astype(int))[~np.repeat(grp, 32, axis=-1)] <= 1)
+    # finer levels put more entries near a decision boundary than INT2 does
+    e2, _ = quant.near_boundary_flags(x, r, 2.0, kappa=2.0 ** -16)
+    assert elem.mean() >= e2.mean() and elem.mean() < 0.05
