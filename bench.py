@@ -161,12 +161,14 @@ def kernel_source_hash():
 
 # ------------------------------------------------------------- byte accounting
 
-def token_bytes(d):
-    return 3 * d // 4, 4 * d          # INT2 token-head (K+V codes + fp16 s/z), BF16 token-head
+def token_bytes(d, bits=2):
+    """(code token-head bytes: K+V codes + fp16 s/z; BF16 token-head bytes).
+    INT2: 3d/4; the INT4 variant: 5d/4."""
+    return (bits + 1) * d // 4, 4 * d
 
 
-def attention_bytes(lens, hkv, hq, d, sink, window, bf16_only=False):
-    i2, bf = token_bytes(d)
+def attention_bytes(lens, hkv, hq, d, sink, window, bf16_only=False, bits=2):
+    i2, bf = token_bytes(d, bits)
     tot = 0
     for L in lens:
         L = int(L)
@@ -179,8 +181,8 @@ def attention_bytes(lens, hkv, hq, d, sink, window, bf16_only=False):
     return tot
 
 
-def append_bytes(lens, hkv, d, sink, window, bf16_only=False):
-    i2, bf = token_bytes(d)
+def append_bytes(lens, hkv, d, sink, window, bf16_only=False, bits=2):
+    i2, bf = token_bytes(d, bits)
     tot = 0
     for L in lens:
         tot += hkv * (bf + bf)                  # read new token, write it to its BF16 slot
@@ -243,7 +245,7 @@ def clone_cache(c):
 class Decoder:
     """One set of layer caches plus the per-step calls (INT2 mixed or BF16-only)."""
 
-    def __init__(self, di, rot, dev, *, bf16_only=False, l2_bytes=0):
+    def __init__(self, di, rot, dev, *, bf16_only=False, l2_bytes=0, code_bits=2):
         import torch
         from int2_rotated_kv_gb300 import _lib as L
         w = di.workload
@@ -261,15 +263,15 @@ class Decoder:
                         shared_prefix_tokens=w.shared_prefix)
         rk, rv, ck, cv = rot
         base = pages.allocate(pp, hkv=hkv, hq=hq, d=d, sink=self.S, window=self.W, device=dev,
-                              r_k=rk, r_v=rv, clip_k=ck, clip_v=cv)
+                              r_k=rk, r_v=rv, clip_k=ck, clip_v=cv, code_bits=code_bits)
         L.oscar_prefill_quantize(base, di.k_tok, di.v_tok, di.seq_ids, di.positions,
                                  torch.tensor((self.lens - 1).astype(np.int32), device=dev))
         torch.cuda.synchronize()
         self.layer_bytes = (base.int2_pool.numel() + base.bf16_pool.numel() * 2)
-        self.step_bytes = attention_bytes(self.lens, hkv, hq, d, self.S, self.W, bf16_only)
+        self.step_bytes = attention_bytes(self.lens, hkv, hq, d, self.S, self.W, bf16_only, code_bits)
         self.attn_bytes = self.step_bytes
-        self.step_bytes += append_bytes(self.lens, hkv, d, self.S, self.W, bf16_only)
-        touched = attention_bytes(self.lens, hkv, hq, d, self.S, self.W, bf16_only)
+        self.step_bytes += append_bytes(self.lens, hkv, d, self.S, self.W, bf16_only, code_bits)
+        touched = self.attn_bytes
         n_layers = max(2, math.ceil(3 * l2_bytes / max(touched, 1)) + 1) if l2_bytes else 1
         self.caches = [base] + [clone_cache(base) for _ in range(n_layers - 1)]
         self.k_new, self.v_new, self.q = di.k_new, di.v_new, di.q
@@ -550,11 +552,11 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------- extras
 
-def decode_leg(di, rot, dev, l2, steps=200, warmup=10, bf16_only=False):
+def decode_leg(di, rot, dev, l2, steps=200, warmup=10, bf16_only=False, code_bits=2):
     """One layer's decode step (append + attention) at di's shape: µs, GB/s,
     and the decode call alone."""
     torch = __import__("torch")
-    dec = Decoder(di, rot, dev, bf16_only=bf16_only, l2_bytes=l2)
+    dec = Decoder(di, rot, dev, bf16_only=bf16_only, l2_bytes=l2, code_bits=code_bits)
     t, clk = time_steps(dec, steps, warmup, clocks=Clocks(torch.cuda.current_device()))
     med, mean = time_decode_calls(dec, 100)
     res = {"batch": len(di.seq_lens), "us_per_layer_step": round(t * 1e3, 3),
@@ -703,13 +705,46 @@ def extra_calibration(dev, l2, n_calib=8192):
     return res
 
 
-def pool_bytes_per_seq(w, L, bf16_only):
+def pool_bytes_per_seq(w, L, bf16_only, code_bits=2):
     """Allocated page-slot bytes of one sequence of L tokens in one layer (the
     same page plan the decoder allocates: cache filled to L - 1 plus one page of growth)."""
     S, W = (0, L + 1) if bf16_only else (w.sink, w.window)
     pp = pages.plan(np.array([L - 1]), S, W, growth=1)
     d, H = w.head_dim, w.num_kv_heads
-    return pp.num_int2_pages * H * 12 * d + pp.num_bf16_pages * H * 64 * d
+    return (pp.num_int2_pages * pages.int2_bytes_per_page(H, d, code_bits)
+            + pp.num_bf16_pages * pages.bf16_bytes_per_page(H, d))
+
+
+def extra_int4(dev, l2, n_calib, budget=40e9):
+    """The INT4 variant (16 levels, two 2-bit planes) beside INT2: the Qwen3-8B
+    32k and Qwen3-32B 128k steps at batch 1, and the batch and tokens/s that fit
+    the 40e9-byte budget at L = 4096 (36 layers, one timed)."""
+    torch = __import__("torch")
+    res = {}
+    for w in (synth.QWEN3_8B_32K, synth.QWEN3_32B_128K):
+        di = synth.draw_device(w, w.seq_lens(), dev, n_calib=n_calib)
+        rot = calibrate_with_library(di, n_calib)
+        r4 = decode_leg(di, rot, dev, l2, code_bits=4)
+        r2 = decode_leg(di, rot, dev, l2)
+        r4.pop("clocks", None)
+        r4["int2_us_per_layer_step"] = r2["us_per_layer_step"]
+        r4["int4_over_int2_time"] = round(r4["us_per_layer_step"] / r2["us_per_layer_step"], 3)
+        res[w.name] = r4
+        del di
+        torch.cuda.empty_cache()
+    w = synth.QWEN3_8B_BUDGET
+    Lc, layers = int(w.context), w.layers
+    per_i4 = pool_bytes_per_seq(w, Lc, False, 4) * layers
+    b_i4 = int(budget // per_i4)
+    di = synth.draw_device(w, np.full(b_i4, Lc), dev, n_calib=n_calib)
+    rot = calibrate_with_library(di, n_calib)
+    r = decode_leg(di, rot, dev, l2, steps=100, warmup=5, code_bits=4)
+    r.pop("clocks", None)
+    r["tokens_per_s"] = round(b_i4 / (layers * r["us_per_layer_step"] * 1e-6), 1)
+    res["budget40GB_L4096"] = {"int4_bytes_per_seq": per_i4, "int4_batch": b_i4, "int4": r}
+    del di
+    torch.cuda.empty_cache()
+    return res
 
 
 def extra_budget(dev, l2, n_calib, budget=40e9):
@@ -796,6 +831,7 @@ EXTRA_LEGS = {
     synth.QWEN3_8B_BUDGET.name: extra_budget,
     "qwen3_8b_32k_chunk16": extra_multiquery,
     "qwen3_8b_calibration_8192": lambda dev, l2, _n: extra_calibration(dev, l2, 8192),
+    "int4_variant": extra_int4,
 }
 
 

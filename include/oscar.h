@@ -49,6 +49,14 @@
  * Stored INT2 values are, per group of 32 rotated channels, code*s + z with
  * s = fp16((max-min)/3), z = fp16(min) of the clipped group and
  * code = round-half-even((y_clipped - z)/s) in [0, 3] (0 when s == 0).
+ *
+ * INT4 variant (desc->code_bits = 4; a format beside the pages' INT2, for the
+ * comparison with INT4 caches in [Summary 4]): sixteen levels, s = fp16((max -
+ * min)/15), codes in [0, 15].  A code c is stored as two 2-bit planes, c >> 2
+ * in plane 0 and c & 3 in plane 1, each in the INT2 code order; the block of a
+ * (page, head) is 20*d bytes: key planes (2 x 4d B), key (scale, zero) pairs
+ * (2d B), value planes (2 x 4d B), value scales (d B) and zeros (d B).  Every
+ * device call accepts either width; the BF16 pool is the same.
  */
 #ifndef OSCAR_H_
 #define OSCAR_H_
@@ -95,6 +103,7 @@ typedef struct oscar_cache_desc {
   const float* clip_k;             /* device [num_kv_heads]                           */
   const float* clip_v;             /* device [num_kv_heads]                           */
   int32_t* status;                 /* optional device word (OSCAR_DEVERR_* bits)      */
+  int32_t code_bits;               /* 2 (or 0): INT2 pages; 4: the INT4 variant       */
 } oscar_cache_desc;
 
 /* ---------------------------------------------------------------- host calls */

@@ -206,6 +206,7 @@ inline oscar_status check_desc(const oscar_cache_desc* c, bool needs_int2, bool 
       c->max_pages_per_seq < 1)
     return OSCAR_ERR_INVALID_ARG;
   if (!head_dim_ok(c->head_dim)) return OSCAR_ERR_UNSUPPORTED;
+  if (c->code_bits != 0 && c->code_bits != 2 && c->code_bits != 4) return OSCAR_ERR_UNSUPPORTED;
   if (c->num_q_heads % c->num_kv_heads) return OSCAR_ERR_INVALID_ARG;
   const int g = c->num_q_heads / c->num_kv_heads;
   if (!(g == 1 || g == 2 || g == 4 || g == 8 || g == 16)) return OSCAR_ERR_UNSUPPORTED;
@@ -220,6 +221,9 @@ inline oscar_status check_desc(const oscar_cache_desc* c, bool needs_int2, bool 
     return OSCAR_ERR_INVALID_ARG;   // rotations are staged by 16-byte bulk copies
   return OSCAR_OK;
 }
+
+// 2-bit code planes of the cache: 1 (INT2) or 2 (the INT4 variant)
+inline int code_planes(const oscar_cache_desc* c) { return c->code_bits == 4 ? 2 : 1; }
 
 int sm_count();
 

@@ -122,11 +122,13 @@ __global__ void __launch_bounds__(1024) qrot_kernel(const DecodeParams p) {
 
 // ---------------------------------------------------------------- split-K
 
-template <int D, bool kBf16Only>
+// P: 2-bit code planes of the cache (1: INT2; 2: the INT4 variant, whose 20d
+// blocks allow four ring stages per warp at two CTAs per SM)
+template <int D, bool kBf16Only, int P = 1>
 struct SplitCfg {
-  static constexpr int kStagesI = 6;                     // INT2 ring depth per warp
+  static constexpr int kStagesI = P == 2 ? 4 : 6;        // code-page ring depth per warp
   static constexpr int kStagesB = kBf16Only ? 3 : 1;     // BF16 ring depth per warp
-  static constexpr int kRingI = kDWarps * kStagesI * Fmt<D>::kInt2Block;
+  static constexpr int kRingI = kDWarps * kStagesI * Fmt<D, P>::kInt2Block;
   static constexpr int kRingB = kDWarps * kStagesB * Fmt<D>::kBf16Block;
   static constexpr int kRing = kBf16Only ? kRingB : (kRingI > kRingB ? kRingI : kRingB);
   static constexpr int kScratch = kDWarps * (16 + 8 * D) * 4;
@@ -246,20 +248,30 @@ __device__ __forceinline__ bool wait_stage(uint64_t* wbar, int s, uint32_t& phas
 
 // q.K for one INT2 page-head staged at st: log2-domain logits in the m16n8
 // accumulator layout (rows = tokens gid / gid+8, cols = query heads 2tig / 2tig+1).
-template <int D>
+// A lane's code words of one plane (d/32 words: one per 32-channel group).
+template <int NG>
+__device__ __forceinline__ void load_words(const uint8_t* base, int lane, uint32_t (&w)[NG]) {
+  if constexpr (NG == 4) {
+    const uint4 v = reinterpret_cast<const uint4*>(base)[lane];
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else {
+    const uint2 v = reinterpret_cast<const uint2*>(base)[lane];
+    w[0] = v.x; w[1] = v.y;
+  }
+}
+
+// q.K for one code page-head.  P = 2 (INT4 variant): the code is 4 * hi + lo,
+// each plane read as INT2 codes; the high plane's dot products weigh 4.
+template <int D, int P>
 __device__ __forceinline__ void int2_qk(const uint8_t* st, const uint2* qbs, uint32_t qz, float ks,
                                         int lane, float (&lg)[4]) {
+  using F = Fmt<D, P>;
   constexpr int NG = D / 32;
   const int gid = lane >> 2, tig = lane & 3;
-  uint32_t kw[NG];
-  if constexpr (NG == 4) {
-    const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kKc)[lane];
-    kw[0] = v.x; kw[1] = v.y; kw[2] = v.z; kw[3] = v.w;
-  } else {
-    const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kKc)[lane];
-    kw[0] = v.x; kw[1] = v.y;
-  }
-  const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kKsz);
+  uint32_t kw[P][NG];
+#pragma unroll
+  for (int pl = 0; pl < P; ++pl) load_words<NG>(st + F::kKc + pl * F::kPlane, lane, kw[pl]);
+  const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + F::kKsz);
   uint32_t za = 0, zb = 0;
   if (tig < NG) {
     const uint32_t e0 = ksz[gid * NG + tig], e1 = ksz[(gid + 8) * NG + tig];
@@ -283,13 +295,22 @@ __device__ __forceinline__ void int2_qk(const uint8_t* st, const uint2* qbs, uin
   for (int m = 0; m < NG; ++m) {
     // pair (s, i) sits at bits 4s+2i (+16); s = 2, 3 are reached with one shift
     // by 8, so every extracted half is code * 4^i * 16^(s&1) * 2^-24
-    const uint32_t wl = kw[m], wh = kw[m] >> 8;
     const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
     const uint2 b0 = qbs[(2 * m) * 32 + lane], b1 = qbs[(2 * m + 1) * 32 + lane];
     float dg[4];
-    // A registers a0..a3 hold key pairs s = 0, 2, 1, 3
-    mma_f16_z(dg, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
-    mma_f16(dg, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+    {   // A registers a0..a3 hold key pairs s = 0, 2, 1, 3 (lowest plane)
+      const uint32_t wl = kw[P - 1][m], wh = kw[P - 1][m] >> 8;
+      mma_f16_z(dg, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
+      mma_f16(dg, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+    }
+    if constexpr (P == 2) {   // high plane: code bits 3..2
+      const uint32_t wl = kw[0][m], wh = kw[0][m] >> 8;
+      float dh[4];
+      mma_f16_z(dh, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
+      mma_f16(dh, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dg[k] = fmaf(4.f, dh[k], dg[k]);
+    }
     const float fa = half_lo(sa[m]) * ks, fb = half_lo(sb[m]) * ks;
     lg[0] = fmaf(fa, dg[0], lg[0]);
     lg[1] = fmaf(fa, dg[1], lg[1]);
@@ -300,25 +321,24 @@ __device__ __forceinline__ void int2_qk(const uint8_t* st, const uint2* qbs, uin
 
 // p.V for one INT2 page-head: o (channel x query head) += codes^T (p * s), plus
 // the zero term and, on the spare row NG, the probability sum (ones row).
-template <int D>
+template <int D, int P>
 __device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4], int lane,
                                         float (&o)[D / 16][4], float (&zacc)[4]) {
+  using F = Fmt<D, P>;
   constexpr int NG = D / 32;
   const int gid = lane >> 2, tig = lane & 3;
   const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0], pr[1]));
   const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2], pr[3]));
-  uint32_t vw[NG], vs0[NG], vs1[NG];
-  const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVs);
+  uint32_t vw[P][NG], vs0[NG], vs1[NG];
+#pragma unroll
+  for (int pl = 0; pl < P; ++pl) load_words<NG>(st + F::kVc + pl * F::kPlane, lane, vw[pl]);
+  const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + F::kVs);
   if constexpr (NG == 4) {
-    const uint4 v = reinterpret_cast<const uint4*>(st + Fmt<D>::kVc)[lane];
-    vw[0] = v.x; vw[1] = v.y; vw[2] = v.z; vw[3] = v.w;
     const uint4 a = reinterpret_cast<const uint4*>(vsw)[tig * 2];
     const uint4 c = reinterpret_cast<const uint4*>(vsw)[tig * 2 + 1];
     vs0[0] = a.x; vs0[1] = a.y; vs0[2] = a.z; vs0[3] = a.w;
     vs1[0] = c.x; vs1[1] = c.y; vs1[2] = c.z; vs1[3] = c.w;
   } else {
-    const uint2 v = reinterpret_cast<const uint2*>(st + Fmt<D>::kVc)[lane];
-    vw[0] = v.x; vw[1] = v.y;
     const uint2 a = reinterpret_cast<const uint2*>(vsw)[tig * 2];
     const uint2 c = reinterpret_cast<const uint2*>(vsw)[tig * 2 + 1];
     vs0[0] = a.x; vs0[1] = a.y;
@@ -329,13 +349,23 @@ __device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4],
     const uint32_t bb0 = hmul2_u32(pb0, vs0[m]);
     const uint32_t bb1 = hmul2_u32(pb1, vs1[m]);
     // value pair s = r: rows gid (s = 0, 2) read at 4^i, rows gid+8 (s = 1, 3) at 16 * 4^i
-    const uint32_t wl = vw[m], wh = vw[m] >> 8;
     const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
-    mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bb0, bb1);
-    mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
-            bb0, bb1);
+    {   // lowest plane
+      const uint32_t wl = vw[P - 1][m], wh = vw[P - 1][m] >> 8;
+      mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bb0, bb1);
+      mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
+              bb0, bb1);
+    }
+    if constexpr (P == 2) {   // high plane, weighed by 4 (exact in fp16)
+      const uint32_t four = 0x44004400u;
+      const uint32_t bh0 = hmul2_u32(bb0, four), bh1 = hmul2_u32(bb1, four);
+      const uint32_t wl = vw[0][m], wh = vw[0][m] >> 8;
+      mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bh0, bh1);
+      mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
+              bh0, bh1);
+    }
   }
-  const uint32_t* vz = reinterpret_cast<const uint32_t*>(st + Fmt<D>::kVz);
+  const uint32_t* vz = reinterpret_cast<const uint32_t*>(st + F::kVz);
   uint32_t za0 = 0, za2 = 0;
   if (gid < NG) {
     za0 = vz[(tig * 2) * NG + gid];
@@ -350,7 +380,7 @@ __device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4],
 // w, w + 8, ... through its own ring of NS bulk-copied page-head blocks, two
 // pages per step so their dependency chains overlap and share one softmax
 // update.  Invalid page ids (negative) copy page 0 and are masked out.
-template <int D, int NS>
+template <int D, int NS, int P>
 __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, int lo, int n, int L, uint8_t* ring,
                                            uint64_t* bars, uint2* qbs, float (&o)[D / 16][4],
@@ -358,7 +388,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
                                            int lim) {
   static_assert(NS % 2 == 0, "pages are consumed in pairs of stages");
   constexpr int NG = D / 32, NK = D / 16;
-  constexpr int SB = Fmt<D>::kInt2Block;
+  constexpr int SB = Fmt<D, P>::kInt2Block;
   const int gid = lane >> 2, tig = lane & 3, G = p.gq;
   uint8_t* wring = ring + warp * NS * SB;
   uint64_t* wbar = bars + warp * 8;
@@ -447,8 +477,8 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     const uint8_t* stA = wring + s * SB;
     const uint8_t* stB = stA + SB;
     float la[4], lb[4];
-    int2_qk<D>(stA, qbs, qz, ks, lane, la);
-    int2_qk<D>(stB, qbs, qz, ks, lane, lb);
+    int2_qk<D, P>(stA, qbs, qz, ks, lane, la);
+    int2_qk<D, P>(stB, qbs, qz, ks, lane, lb);
     const int pA = (lo + warp + kDWarps * i) * kPage, pB = pA + kDWarps * kPage;
     if (pA < tok_lo || pB + kPage > tok_hi || (idA | idB) < 0) {
       const int t0 = pA + gid, t1 = t0 + 8, u0 = pB + gid, u1 = u0 + 8;
@@ -459,8 +489,8 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     }
     float pa[4], pbv[4];
     softmax_pair<NK>(sm, la, lb, o, zacc, pa, pbv);
-    int2_pv<D>(stA, pa, lane, o, zacc);
-    int2_pv<D>(stB, pbv, lane, o, zacc);
+    int2_pv<D, P>(stA, pa, lane, o, zacc);
+    int2_pv<D, P>(stB, pbv, lane, o, zacc);
     __syncwarp();
     if (lane == 0) {
       if (i + NS < my_n) {
@@ -480,7 +510,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
     const uint8_t* stA = wring + s * SB;
     float la[4];
-    int2_qk<D>(stA, qbs, qz, ks, lane, la);
+    int2_qk<D, P>(stA, qbs, qz, ks, lane, la);
     const int pA = (lo + warp + kDWarps * i) * kPage;
     const int t0 = pA + gid, t1 = t0 + 8;
     if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
@@ -488,7 +518,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     float pa[4];
     float dummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, pd[4];
     softmax_pair<NK>(sm, la, dummy, o, zacc, pa, pd);
-    int2_pv<D>(stA, pa, lane, o, zacc);
+    int2_pv<D, P>(stA, pa, lane, o, zacc);
   }
 }
 
@@ -593,10 +623,10 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
   }
 }
 
-template <int D, bool kBf16Only>
-__global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
+template <int D, bool kBf16Only, int P>
+__global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPerSm)
     split_kernel(const DecodeParams p) {
-  using C = SplitCfg<D, kBf16Only>;
+  using C = SplitCfg<D, kBf16Only, P>;
   constexpr int NG = D / 32;     // groups = code words per lane
   constexpr int NK = D / 16;     // k-steps / channel tiles
   extern __shared__ __align__(128) uint8_t smem[];
@@ -698,7 +728,7 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only>::kCtasPerSm)
   // the INT2 page receiving the token that leaves the window in this step
   const int defer_lp = (p.after_append && L - 1 - p.window >= p.sink) ? (L - 1 - p.window) / kPage : -1;
   if (mode == 0)
-    int2_pages<D, C::kStagesI>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
+    int2_pages<D, C::kStagesI, P>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
                                reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp, qh0, lim);
   else
     bf16_pages<D, C::kStagesB, !kBf16Only>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm, qh0,
@@ -955,10 +985,10 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int D, bool kBf16Only>
+template <int D, bool kBf16Only, int P>
 oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) {
-  using C = SplitCfg<D, kBf16Only>;
-  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(split_kernel<D, kBf16Only>), C::kBytes))
+  using C = SplitCfg<D, kBf16Only, P>;
+  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(split_kernel<D, kBf16Only, P>), C::kBytes))
     return OSCAR_ERR_CUDA;
   const dim3 sgrid(pl.n_splits, p.hkv * p.halves, p.batch);
   cudaError_t e;
@@ -970,9 +1000,9 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
       e = launch_pdl(qrot_kernel<D>, dim3(p.hkv * p.halves, p.batch), dim3(1024), 0, st, p);
       if (e != cudaSuccess) return OSCAR_ERR_CUDA;
     }
-    e = launch_pdl(split_kernel<D, kBf16Only>, sgrid, dim3(kDThreads), C::kBytes, st, p);
+    e = launch_pdl(split_kernel<D, kBf16Only, P>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   } else {
-    e = launch_pdl(split_kernel<D, kBf16Only>, sgrid, dim3(kDThreads), C::kBytes, st, p);
+    e = launch_pdl(split_kernel<D, kBf16Only, P>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   }
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   e = launch_pdl(combine_kernel<D, kBf16Only>, dim3(p.G, p.hkv, p.batch), dim3(256), 0, st, p);
@@ -1041,9 +1071,13 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
     const oscar_status a = append_with_query(c, q, k_new, v_new, seq_lens, batch, p.qrot, st);
     if (a != OSCAR_OK) return a;
   }
-  if (c->head_dim == 128)
-    return bf16_only ? run_decode<128, true>(p, pl, st) : run_decode<128, false>(p, pl, st);
-  return bf16_only ? run_decode<64, true>(p, pl, st) : run_decode<64, false>(p, pl, st);
+  const bool int4 = oscar_host::code_planes(c) == 2;
+  if (c->head_dim == 128) {
+    if (bf16_only) return run_decode<128, true, 1>(p, pl, st);
+    return int4 ? run_decode<128, false, 2>(p, pl, st) : run_decode<128, false, 1>(p, pl, st);
+  }
+  if (bf16_only) return run_decode<64, true, 1>(p, pl, st);
+  return int4 ? run_decode<64, false, 2>(p, pl, st) : run_decode<64, false, 1>(p, pl, st);
 }
 
 }  // namespace oscar

@@ -26,23 +26,31 @@
 // (s, i) sits at bits (4s+2i, 16+4s+2i), so (w >> 4s) & (0x00030003 << 2i) is
 // a half2 whose halves are the two codes times 4^i, read as fp16 subnormals
 // (code * 4^i * 2^-24): exact tensor-core operands without any conversion.
+//
+// INT4 variant (P = 2 planes): a 4-bit code c is kept as two 2-bit planes, the
+// high bits c >> 2 in plane 0 and the low bits c & 3 in plane 1, each plane a
+// code area in exactly the order above.  Block (20*d bytes): Kc plane 0 [0,4d)
+// | Kc plane 1 [4d,8d) | Ksz [8d,10d) | Vc planes [10d,18d) | Vs [18d,19d) |
+// Vz [19d,20d).  The decode kernel runs the INT2 fragment arithmetic on both
+// planes and weighs the high plane by 4.
 #pragma once
 
 #include <stdint.h>
 
 namespace oscar {
 
-template <int D>
+template <int D, int P = 1>
 struct Fmt {
   static constexpr int kNG = D / 32;          // groups per token
   static constexpr int kNK = D / 16;          // 16-channel k-steps / tiles
   static constexpr int kWords = D / 32;       // code words per lane
-  static constexpr int kInt2Block = 12 * D;
-  static constexpr int kKc = 0;
-  static constexpr int kKsz = 4 * D;
-  static constexpr int kVc = 6 * D;
-  static constexpr int kVs = 10 * D;
-  static constexpr int kVz = 11 * D;
+  static constexpr int kPlane = 4 * D;        // bytes of one 2-bit code plane
+  static constexpr int kInt2Block = (8 * P + 4) * D;   // code block (12d INT2, 20d INT4)
+  static constexpr int kKc = 0;               // key plane q at kKc + q * kPlane
+  static constexpr int kKsz = 4 * D * P;
+  static constexpr int kVc = 4 * D * P + 2 * D;   // value plane q at kVc + q * kPlane
+  static constexpr int kVs = 8 * D * P + 2 * D;
+  static constexpr int kVz = 8 * D * P + 3 * D;
   static constexpr int kBf16Block = 64 * D;   // bytes
   static constexpr int kBf16V = 32 * D;       // byte offset of the value half
 };

@@ -53,6 +53,7 @@ struct QuantParams {
   const uint16_t* q;     // [B][Hq][D] bf16
   float* qrot;           // [B][Hq][D] fp32, or null
   int hq, G;
+  int planes;            // 2-bit code planes: 1 (INT2) or 2 (the INT4 variant)
 };
 
 template <int D>
@@ -77,10 +78,13 @@ __device__ __forceinline__ void flag(int32_t* status, int bit) {
 
 namespace oscar {
 
-template <int D>
+template <int D, int P>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   using S = QuantSmem<D>;
+  using F = Fmt<D, P>;
+  constexpr float kLevels = P == 2 ? 15.f : 3.f;   // largest code: INT4 variant / INT2
+  constexpr int kMaxCode = P == 2 ? 15 : 3;
   constexpr int NG = D / 32;
   constexpr int NW = D / 32;    // code words per lane
   float* rs = reinterpret_cast<float*>(smem + S::kR);
@@ -261,14 +265,14 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
       const float yc = fminf(fmaxf(y, -clip), clip);
       const float mn = warp_min(yc);
       const float mx = warp_max(yc);
-      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), kLevels));
       const __half z16 = __float2half_rn(mn);
       const float sf = __half2float(s16);
       const float zf = __half2float(z16);
       int code = 0;
       if (sf != 0.f) {
         code = __float2int_rn(__fdiv_rn(__fsub_rn(yc, zf), sf));
-        code = min(max(code, 0), 3);
+        code = min(max(code, 0), kMaxCode);
       }
       codes[t * D + 32 * grp + lane] = static_cast<uint8_t>(code);
       if (lane == 0)
@@ -277,13 +281,16 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
     }
     __syncthreads();
 
-    // --- pack: one thread per (token, code byte)
-    for (int idx = tid; idx < kQTile * (D / 4); idx += kQThreads) {
-      const int t = idx / (D / 4), q = idx % (D / 4);
+    // --- pack: one thread per (token, code plane, code byte); plane 0 holds the
+    // highest two bits of each code
+    for (int idx = tid; idx < kQTile * P * (D / 4); idx += kQThreads) {
+      const int t = idx / (P * (D / 4)), rem = idx % (P * (D / 4));
+      const int pl = rem / (D / 4), q = rem % (D / 4);
+      const int shift = 2 * (P - 1 - pl);
       const int pg = m_i2page[t];
       if (pg < 0) continue;
       const int slot = m_i2slot[t];
-      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(pg) * p.hkv + h) * Fmt<D>::kInt2Block;
+      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(pg) * p.hkv + h) * F::kInt2Block;
       const uint8_t* ct = codes + t * D;
       uint32_t byte = 0;
       if (kv == 0) {
@@ -292,16 +299,18 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int i = 0; i < 2; ++i)
-            byte |= static_cast<uint32_t>(ct[16 * (2 * m + i) + 8 * hh + 2 * tig + e]) << (4 * hh + 2 * i);
-        blk[Fmt<D>::kKc + key_byte<D>(slot, tig, m, e)] = static_cast<uint8_t>(byte);
+            byte |= ((static_cast<uint32_t>(ct[16 * (2 * m + i) + 8 * hh + 2 * tig + e]) >> shift) & 3u)
+                    << (4 * hh + 2 * i);
+        blk[F::kKc + pl * F::kPlane + key_byte<D>(slot, tig, m, e)] = static_cast<uint8_t>(byte);
       } else {
         const int gid = q / NW, m = q % NW;
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
           for (int i = 0; i < 2; ++i)
-            byte |= static_cast<uint32_t>(ct[16 * (2 * m + i) + 8 * ch + gid]) << (4 * ch + 2 * i);
-        blk[Fmt<D>::kVc + value_byte<D>(slot, gid, m)] = static_cast<uint8_t>(byte);
+            byte |= ((static_cast<uint32_t>(ct[16 * (2 * m + i) + 8 * ch + gid]) >> shift) & 3u)
+                    << (4 * ch + 2 * i);
+        blk[F::kVc + pl * F::kPlane + value_byte<D>(slot, gid, m)] = static_cast<uint8_t>(byte);
       }
     }
     for (int idx = tid; idx < kQTile * NG; idx += kQThreads) {
@@ -309,24 +318,24 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
       const int pg = m_i2page[t];
       if (pg < 0) continue;
       const int slot = m_i2slot[t];
-      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(pg) * p.hkv + h) * Fmt<D>::kInt2Block;
+      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(pg) * p.hkv + h) * F::kInt2Block;
       const uint32_t sz = szs[t * NG + grp];
       if (kv == 0) {
-        reinterpret_cast<uint32_t*>(blk + Fmt<D>::kKsz)[slot * NG + grp] = sz;
+        reinterpret_cast<uint32_t*>(blk + F::kKsz)[slot * NG + grp] = sz;
       } else {
         const int e = vsz_index<D>(slot, grp);
-        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
-        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVz)[e] = static_cast<uint16_t>(sz >> 16);
+        reinterpret_cast<uint16_t*>(blk + F::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
+        reinterpret_cast<uint16_t*>(blk + F::kVz)[e] = static_cast<uint16_t>(sz >> 16);
       }
     }
   }
   if (!r_ready) mbar_wait(bar, 0, p.status);   // never leave with the copy in flight
 }
 
-template <int D>
-oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
+template <int D, int P>
+oscar_status launch_quantize_p(const QuantParams& p, cudaStream_t st) {
   const int smem = QuantSmem<D>::kBytes;
-  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(quantize_kernel<D>), smem))
+  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(quantize_kernel<D, P>), smem))
     return OSCAR_ERR_CUDA;
   const int64_t tiles = (p.n_items + kQTile - 1) / kQTile;
   if (tiles == 0) return OSCAR_OK;
@@ -343,7 +352,12 @@ oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, quantize_kernel<D>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<D, P>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+template <int D>
+oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
+  return p.planes == 2 ? launch_quantize_p<D, 2>(p, st) : launch_quantize_p<D, 1>(p, st);
 }
 
 // ------------------------------------------------------------------ append
@@ -357,9 +371,12 @@ oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
 // and a warp handles one sequence (lane j = output channel 32*grp + j).
 constexpr int kAppendSeqs = 8;      // sequences per CTA: one per warp
 
-template <int D>
+template <int D, int P>
 __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) {
   constexpr int NG = D / 32;
+  using F = Fmt<D, P>;
+  constexpr float kLevels = P == 2 ? 15.f : 3.f;   // largest code: INT4 variant / INT2
+  constexpr int kMaxCode = P == 2 ? 15 : 3;
   __shared__ __align__(16) float rs[D][32];          // R[:, 32*grp .. 32*grp + 31]
   __shared__ __align__(16) float xs[kQThreads / 32][D];
   __shared__ uint8_t cs[kQThreads / 32][32];
@@ -456,52 +473,55 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
     const float yc = fminf(fmaxf(y, -clip), clip);
     const float mn = warp_min(yc);
     const float mx = warp_max(yc);
-    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), kLevels));
     const __half z16 = __float2half_rn(mn);
     const float sf = __half2float(s16);
     const float zf = __half2float(z16);
     int code = 0;
-    if (sf != 0.f) code = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(yc, zf), sf)), 0), 3);
+    if (sf != 0.f) code = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(yc, zf), sf)), 0), kMaxCode);
     cs[warp][lane] = static_cast<uint8_t>(code);
     __syncwarp();
-    uint8_t* blk = p.int2_pool + (static_cast<int64_t>(dp) * p.hkv + h) * Fmt<D>::kInt2Block;
+    uint8_t* blk = p.int2_pool + (static_cast<int64_t>(dp) * p.hkv + h) * F::kInt2Block;
     const uint8_t* ct = cs[warp];
-    if (lane < 8) {   // 8 code bytes of this group
+    if (lane < 8 * P) {   // 8 code bytes of this group per plane; plane 0 = highest bits
+      const int pl = lane >> 3, lb = lane & 7, shift = 2 * (P - 1 - pl);
       uint32_t byte = 0;
       if (kv == 0) {
-        const int tig = lane >> 1, e = lane & 1;
+        const int tig = lb >> 1, e = lb & 1;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int i = 0; i < 2; ++i)
-            byte |= static_cast<uint32_t>(ct[16 * i + 8 * hh + 2 * tig + e]) << (4 * hh + 2 * i);
-        blk[Fmt<D>::kKc + key_byte<D>(slot, tig, grp, e)] = static_cast<uint8_t>(byte);
+            byte |= ((static_cast<uint32_t>(ct[16 * i + 8 * hh + 2 * tig + e]) >> shift) & 3u)
+                    << (4 * hh + 2 * i);
+        blk[F::kKc + pl * F::kPlane + key_byte<D>(slot, tig, grp, e)] = static_cast<uint8_t>(byte);
       } else {
-        const int gid = lane;
+        const int gid = lb;
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
           for (int i = 0; i < 2; ++i)
-            byte |= static_cast<uint32_t>(ct[16 * i + 8 * ch + gid]) << (4 * ch + 2 * i);
-        blk[Fmt<D>::kVc + value_byte<D>(slot, gid, grp)] = static_cast<uint8_t>(byte);
+            byte |= ((static_cast<uint32_t>(ct[16 * i + 8 * ch + gid]) >> shift) & 3u)
+                    << (4 * ch + 2 * i);
+        blk[F::kVc + pl * F::kPlane + value_byte<D>(slot, gid, grp)] = static_cast<uint8_t>(byte);
       }
-    } else if (lane == 8) {
+    } else if (lane == 8 * P) {
       const uint32_t sz = static_cast<uint32_t>(__half_as_ushort(s16)) |
                           (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
       if (kv == 0) {
-        reinterpret_cast<uint32_t*>(blk + Fmt<D>::kKsz)[slot * NG + grp] = sz;
+        reinterpret_cast<uint32_t*>(blk + F::kKsz)[slot * NG + grp] = sz;
       } else {
         const int e = vsz_index<D>(slot, grp);
-        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
-        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVz)[e] = static_cast<uint16_t>(sz >> 16);
+        reinterpret_cast<uint16_t*>(blk + F::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
+        reinterpret_cast<uint16_t*>(blk + F::kVz)[e] = static_cast<uint16_t>(sz >> 16);
       }
     }
     __syncwarp();
   }
 }
 
-template <int D>
-oscar_status launch_append(const QuantParams& p, cudaStream_t st) {
+template <int D, int P>
+oscar_status launch_append_p(const QuantParams& p, cudaStream_t st) {
   const int64_t chunks = (p.n_items + kAppendSeqs - 1) / kAppendSeqs;
   if (chunks == 0) return OSCAR_OK;
   const dim3 grid(static_cast<unsigned>(chunks * (D / 32)), p.hkv, 2);
@@ -515,7 +535,12 @@ oscar_status launch_append(const QuantParams& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, append_kernel<D>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, append_kernel<D, P>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+template <int D>
+oscar_status launch_append(const QuantParams& p, cudaStream_t st) {
+  return p.planes == 2 ? launch_append_p<D, 2>(p, st) : launch_append_p<D, 1>(p, st);
 }
 
 QuantParams base_params(const oscar_cache_desc* c) {
@@ -535,6 +560,7 @@ QuantParams base_params(const oscar_cache_desc* c) {
   p.clip_k = c->clip_k;
   p.clip_v = c->clip_v;
   p.status = c->status;
+  p.planes = oscar_host::code_planes(c);
   return p;
 }
 

@@ -164,19 +164,19 @@ __device__ __forceinline__ uint32_t tc_sw128_offset(int row, int k, int rows) {
 
 // ------------------------------------------------------------------ kernel
 
-// Code of one value: rint(fl((y_c - z16) / s16)) clamped to [0, 3], the division
-// correctly rounded.  The product with the reciprocal differs from the quotient
-// by ~1e-6 at most, so it decides the code unless it lies within 4e-6 of a
-// half-integer; there the exact quotient is taken.
-__device__ __forceinline__ int tc_code(float yc, float zf, float sf, float inv) {
+// Code of one value: rint(fl((y_c - z16) / s16)) clamped to [0, max_code], the
+// division correctly rounded.  The product with the reciprocal differs from the
+// quotient by ~1e-6 at most (relative), so it decides the code unless it lies
+// within 4e-6 * (1 + |q|) of a half-integer; there the exact quotient is taken.
+__device__ __forceinline__ int tc_code(float yc, float zf, float sf, float inv, int max_code) {
   const float a = __fsub_rn(yc, zf);
   float q = __fmul_rn(a, inv);
   float r = rintf(q);
-  if (fabsf(fabsf(q - r) - 0.5f) < 4e-6f) r = rintf(__fdiv_rn(a, sf));
-  return min(max(static_cast<int>(r), 0), 3);
+  if (fabsf(fabsf(q - r) - 0.5f) < 4e-6f * (1.f + fabsf(q))) r = rintf(__fdiv_rn(a, sf));
+  return min(max(static_cast<int>(r), 0), max_code);
 }
 
-template <int D>
+template <int D, int P>
 __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
     rotate_tc_kernel(const QuantParams p, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v) {
@@ -398,7 +398,9 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       if (lane == 0) tc_arrive(&acc_empty[buf]);
       if (i2 < 0) continue;
       const int slot = i2 % kPage;
-      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(i2 / kPage) * p.hkv + h) * Fmt<D>::kInt2Block;
+      using F = Fmt<D, P>;
+      constexpr int kMaxCode = P == 2 ? 15 : 3;   // INT4 variant / INT2
+      uint8_t* blk = p.int2_pool + (static_cast<int64_t>(i2 / kPage) * p.hkv + h) * F::kInt2Block;
       float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -406,42 +408,61 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
         mn = fminf(mn, y[j]);
         mx = fmaxf(mx, y[j]);
       }
-      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kMaxCode)));
       const __half z16 = __float2half_rn(mn);
       const float sf = __half2float(s16), zf = __half2float(z16);
       const bool live = sf != 0.f;            // a zero scale gives code 0 everywhere
       const float inv = live ? __fdiv_rn(1.0f, sf) : 0.f;
       auto code = [&](int j) -> uint32_t {
-        return live ? static_cast<uint32_t>(tc_code(y[j], zf, sf, inv)) : 0u;
+        return live ? static_cast<uint32_t>(tc_code(y[j], zf, sf, inv, kMaxCode)) : 0u;
       };
       const uint32_t sz = static_cast<uint32_t>(__half_as_ushort(s16)) |
                           (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
+      // each code is decided once; plane 0 takes its highest two bits
       if (kv == 0) {
 #pragma unroll
         for (int tig = 0; tig < 4; ++tig)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            uint32_t byte = 0;
+            uint32_t c4[4];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-              for (int i = 0; i < 2; ++i) byte |= code(16 * i + 8 * hh + 2 * tig + e) << (4 * hh + 2 * i);
-            blk[Fmt<D>::kKc + key_byte<D>(slot, tig, grp, e)] = static_cast<uint8_t>(byte);
+              for (int i = 0; i < 2; ++i) c4[2 * hh + i] = code(16 * i + 8 * hh + 2 * tig + e);
+#pragma unroll
+            for (int pl = 0; pl < P; ++pl) {
+              const int shift = 2 * (P - 1 - pl);
+              uint32_t byte = 0;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) byte |= ((c4[2 * hh + i] >> shift) & 3u) << (4 * hh + 2 * i);
+              blk[F::kKc + pl * F::kPlane + key_byte<D>(slot, tig, grp, e)] = static_cast<uint8_t>(byte);
+            }
           }
-        reinterpret_cast<uint32_t*>(blk + Fmt<D>::kKsz)[slot * NG + grp] = sz;
+        reinterpret_cast<uint32_t*>(blk + F::kKsz)[slot * NG + grp] = sz;
       } else {
 #pragma unroll
         for (int gid = 0; gid < 8; ++gid) {
-          uint32_t byte = 0;
+          uint32_t c4[4];
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-            for (int i = 0; i < 2; ++i) byte |= code(16 * i + 8 * ch + gid) << (4 * ch + 2 * i);
-          blk[Fmt<D>::kVc + value_byte<D>(slot, gid, grp)] = static_cast<uint8_t>(byte);
+            for (int i = 0; i < 2; ++i) c4[2 * ch + i] = code(16 * i + 8 * ch + gid);
+#pragma unroll
+          for (int pl = 0; pl < P; ++pl) {
+            const int shift = 2 * (P - 1 - pl);
+            uint32_t byte = 0;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+              for (int i = 0; i < 2; ++i) byte |= ((c4[2 * ch + i] >> shift) & 3u) << (4 * ch + 2 * i);
+            blk[F::kVc + pl * F::kPlane + value_byte<D>(slot, gid, grp)] = static_cast<uint8_t>(byte);
+          }
         }
         const int e = vsz_index<D>(slot, grp);
-        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
-        reinterpret_cast<uint16_t*>(blk + Fmt<D>::kVz)[e] = static_cast<uint16_t>(sz >> 16);
+        reinterpret_cast<uint16_t*>(blk + F::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
+        reinterpret_cast<uint16_t*>(blk + F::kVz)[e] = static_cast<uint16_t>(sz >> 16);
       }
     }
   }
@@ -484,8 +505,8 @@ inline bool make_token_map(CUtensorMap* m, const void* base, int64_t rows, int c
 // Launch the tensor-core prefill; returns false (nothing launched) when the
 // inputs do not meet the tensor maps' rules, so the caller can take the
 // CUDA-core kernel instead.
-template <int D>
-bool launch_rotate_tc(const QuantParams& p, cudaStream_t st, oscar_status* result) {
+template <int D, int P>
+bool launch_rotate_tc_p(const QuantParams& p, cudaStream_t st, oscar_status* result) {
   using S = TcSmem<D>;
   if ((reinterpret_cast<uintptr_t>(p.k_src) | reinterpret_cast<uintptr_t>(p.v_src)) & 15)
     return false;
@@ -494,7 +515,7 @@ bool launch_rotate_tc(const QuantParams& p, cudaStream_t st, oscar_status* resul
   if (!make_token_map(&mk, p.k_src, p.n_items, p.hkv * D) ||
       !make_token_map(&mv, p.v_src, p.n_items, p.hkv * D))
     return false;
-  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(rotate_tc_kernel<D>), S::kAlloc)) {
+  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(rotate_tc_kernel<D, P>), S::kAlloc)) {
     *result = OSCAR_ERR_CUDA;
     return true;
   }
@@ -512,10 +533,16 @@ bool launch_rotate_tc(const QuantParams& p, cudaStream_t st, oscar_status* resul
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  *result = cudaLaunchKernelEx(&cfg, rotate_tc_kernel<D>, p, mk, mv) == cudaSuccess
+  *result = cudaLaunchKernelEx(&cfg, rotate_tc_kernel<D, P>, p, mk, mv) == cudaSuccess
                 ? OSCAR_OK
                 : OSCAR_ERR_CUDA;
   return true;
+}
+
+template <int D>
+bool launch_rotate_tc(const QuantParams& p, cudaStream_t st, oscar_status* result) {
+  return p.planes == 2 ? launch_rotate_tc_p<D, 2>(p, st, result)
+                       : launch_rotate_tc_p<D, 1>(p, st, result);
 }
 
 }  // namespace oscar

@@ -52,8 +52,22 @@ def make_cache(inst, rot, *, window, sink=4, growth=0, shared=0, permute=None, l
     return c, pp
 
 
-def prefill(cache, inst, lens=None, upto=None):
-    """Place tokens [0, upto_b) of every sequence (default: all), final length lens."""
+def misaligned_copy(x):
+    """A device copy of x whose data starts 8 bytes past a 16-byte boundary:
+    inputs the tensor-memory-access prefill cannot take, so the library runs its
+    CUDA-core quantiser instead."""
+    t = torch()
+    buf = t.empty(x.numel() + 8, dtype=x.dtype, device=x.device)
+    view = buf[4:4 + x.numel()].view(x.shape)
+    view.copy_(x)
+    assert view.data_ptr() % 16 == 8
+    return view
+
+
+def prefill(cache, inst, lens=None, upto=None, misalign=False):
+    """Place tokens [0, upto_b) of every sequence (default: all), final length lens.
+    misalign: hand the key/value rows over at an address the tensor-core path
+    rejects (the CUDA-core quantiser then places them)."""
     t = torch()
     lens = inst.seq_lens if lens is None else np.asarray(lens)
     ks, vs, sid, pos = [], [], [], []
@@ -66,6 +80,8 @@ def prefill(cache, inst, lens=None, upto=None):
         pos.append(np.arange(n, dtype=np.int32))
     k = bf16_tensor(np.concatenate(ks))
     v = bf16_tensor(np.concatenate(vs))
+    if misalign:
+        k, v = misaligned_copy(k), misaligned_copy(v)
     L = lib()
     L.oscar_prefill_quantize(cache, k, v, t.from_numpy(np.concatenate(sid)).to(DEV),
                              t.from_numpy(np.concatenate(pos)).to(DEV),

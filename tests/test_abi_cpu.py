@@ -114,11 +114,17 @@ def test_argument_errors_before_any_launch(L):
     # shapes outside the supported set
     for bad, want in ((dict(head_dim=96), -2), (dict(num_q_heads=12, num_kv_heads=1), -2),
                       (dict(num_q_heads=6, num_kv_heads=4), -1), (dict(window=0), -1),
-                      (dict(int2_pool=None), -1), (dict(int2_pool=257), -1)):
+                      (dict(int2_pool=None), -1), (dict(int2_pool=257), -1),
+                      (dict(code_bits=3), -2), (dict(code_bits=8), -2)):
         d = _desc(L, **bad)
         st = lib.oscar_decode_attention(ctypes.byref(d), 4096, 4096, 1, 16, 4096, 4096, 1 << 20, None)
         assert st == want, (bad, st)
     assert lib.oscar_decode_attention(None, 1, 1, 1, 1, 1, 1, 1, None) == -1
+    # the INT4 variant (code_bits 4) passes the same checks as INT2 (2, or 0)
+    for bits in (0, 2, 4):
+        d4 = _desc(L, code_bits=bits)
+        assert lib.oscar_decode_attention(ctypes.byref(d4), 4096, 4096, 1, 16, 4096, 4096, 8,
+                                          None) == -3
     # null buffers, bad sizes
     assert lib.oscar_decode_attention(ctypes.byref(ok), None, 4096, 1, 16, 4096, 4096, 1 << 20, None) == -1
     assert lib.oscar_decode_attention(ctypes.byref(ok), 4096, 4096, 1, 0, 4096, 4096, 1 << 20, None) == -1
