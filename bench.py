@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--n-calib", type=int, default=None)
     ap.add_argument("--profile", action="store_true",
                     help="minimal run for ncu: one layer cache, eager steps, no extra legs")
+    ap.add_argument("--code-bits", type=int, default=2, choices=[2, 4],
+                    help="with --profile: the INT4 variant's caches (the headline is INT2)")
     ap.add_argument("--leg", default=None, choices=sorted(EXTRA_LEGS),
                     help="run one extra leg alone and print its JSON (for profiling)")
     return ap.parse_args()
@@ -870,11 +872,12 @@ def main():
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     if args.profile:
         # launches in order: 1 prefill, then per step the fused append (+ q'), split, combine
-        dec = Decoder(device_inputs(inst, dev), rot, dev, l2_bytes=0)
+        dec = Decoder(device_inputs(inst, dev), rot, dev, l2_bytes=0, code_bits=args.code_bits)
         for i in range(args.warmup + args.steps):
             dec.step(i)
         torch.cuda.synchronize()
-        print(json.dumps({"profile": w.name, "steps": args.steps, "warmup": args.warmup,
+        print(json.dumps({"profile": w.name, "code_bits": args.code_bits, "steps": args.steps,
+                          "warmup": args.warmup,
                           "launches_per_step": dec.launches_per_step,
                           "attention_bytes": int(dec.attn_bytes)}), flush=True)
         return
