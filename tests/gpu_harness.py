@@ -134,7 +134,8 @@ def decode(cache, q, lens, max_len=None, bf16_only=False, out=None):
     return from_bf16(o)
 
 
-def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=None, upto=None):
+def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=None, upto=None,
+                         heads=None):
     """The oracle's attention over what the GPU actually stored: every token of
     every sequence read back from the pools (INT2 codes, s16, z16 dequantised and
     rotated back with R^T; BF16 tokens as stored), then fp64 softmax attention.
@@ -142,7 +143,8 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=Non
     near-boundary codes may differ from the oracle's by one step).  ``drop``:
     optional {sequence: logical pages} whose tokens are left out.  ``upto``:
     optional last visible position per sequence (a query row of a chunk).  The
-    code width (INT2 or the INT4 variant) is the cache's ``code_bits``."""
+    code width (INT2 or the INT4 variant) is the cache's ``code_bits``.
+    ``heads``: optional KV heads to compute (the others' outputs stay zero)."""
     got2, gotb = pools(cache)
     B, Hq, d = q.shape
     hkv = Hq // gqa
@@ -154,7 +156,7 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=Non
         L = int(lens[b])
         t = np.arange(L)
         m = ocache.is_int2(t, L, sink, window)
-        for h in range(hkv):
+        for h in (range(hkv) if heads is None else heads):
             k = np.zeros((L, d))
             v = np.zeros((L, d))
             for pg in range((L + 15) // 16):
