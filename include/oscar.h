@@ -235,6 +235,25 @@ oscar_status oscar_decode_step(const oscar_cache_desc* desc, const void* q, cons
                                int32_t max_seq_len, void* out, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* oscar_decode_step with the rotary position embedding of the serving model
+ * applied to the step's new query and key first (the fused pipeline of a
+ * decode layer, [Abstract] "fused kernel pipelines"): for the new token at
+ * position m = seq_lens_after[b] - 1, every head vector x of q and k_new is
+ * rotated pairwise, (x_i, x_{i+d/2}) -> (x_i cos a - x_{i+d/2} sin a,
+ * x_{i+d/2} cos a + x_i sin a), a = m * rope_base^(-2i/d), i < d/2 (the
+ * rotate-half arrangement over the whole head, as in Qwen3), and rounded to
+ * bf16; the rotated key enters the cache, the rotated query attends.  Angles
+ * are formed and reduced modulo 2 pi in fp64, cos/sin and the rotation in fp32.
+ * v_new is not rotated.  Tokens already in the cache are used as stored (they
+ * were rotated when they entered).  rope_base > 1 and finite
+ * (else OSCAR_ERR_INVALID_ARG); the workspace is oscar_decode_workspace_size
+ * bytes, as for oscar_decode_step. */
+oscar_status oscar_decode_step_rope(const oscar_cache_desc* desc, const void* q, const void* k_new,
+                                    const void* v_new, const int32_t* seq_lens_after,
+                                    int32_t batch, int32_t max_seq_len, double rope_base,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
 /* oscar_decode_attention for callers that cannot allocate device memory.
  * The pages describe no counterpart; it exists because some callers have no
  * allocator at hand when they run attention: a plug-in inside a runtime that

@@ -25,7 +25,7 @@ EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rot
             "oscar_prefill_quantize", "oscar_quantize_append", "oscar_decode_workspace_size",
             "oscar_decode_attention", "oscar_decode_attention_bf16", "oscar_device_sm_count",
             "oscar_status_string", "oscar_version", "oscar_decode_attention_static",
-            "oscar_decode_step", "oscar_multiquery_attention",
+            "oscar_decode_step", "oscar_decode_step_rope", "oscar_multiquery_attention",
             "oscar_calibration_workspace_size", "oscar_query_covariance_device",
             "oscar_score_covariance_device", "oscar_clip_threshold_device")
 
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "oscar_device_sm_count": (I32, []),
             "oscar_decode_attention_static": (I32, [P, P, P, I32, I32, P, P]),
             "oscar_decode_step": (I32, [P, P, P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
+            "oscar_decode_step_rope": (I32, [P, P, P, P, P, I32, I32, D, P, P, ctypes.c_size_t, P]),
             "oscar_multiquery_attention": (I32, [P, P, P, P, I32, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_calibration_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I64]),
             "oscar_query_covariance_device": (I32, [I32, I32, I32, I64, P, P, P, ctypes.c_size_t, P]),
@@ -252,6 +253,18 @@ def oscar_decode_step(cache: Cache, q, k_new, v_new, seq_lens_after, max_seq_len
                                    _ptr(seq_lens_after), int(seq_lens_after.numel()),
                                    int(max_seq_len), _ptr(out), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def oscar_decode_step_rope(cache: Cache, q, k_new, v_new, seq_lens_after, max_seq_len: int,
+                           rope_base: float, out, workspace, stream=None):
+    """The fused decode step with the rotary embedding of the new query and key."""
+    d = cache.desc()
+    _check("oscar_decode_step_rope",
+           lib().oscar_decode_step_rope(ctypes.byref(d), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                        _ptr(seq_lens_after), int(seq_lens_after.numel()),
+                                        int(max_seq_len), float(rope_base), _ptr(out),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
 
 
 def oscar_multiquery_attention(cache: Cache, q, seq_lens, q_pos, max_seq_len: int, out, workspace,

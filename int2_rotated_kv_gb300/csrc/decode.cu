@@ -936,7 +936,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
 
 struct Plan {
   int n_main, pps, n_splits;
-  size_t qrot_bytes, part_off, part_bytes, total;
+  size_t qrot_bytes, part_off, part_bytes, qrope_off, total;
 };
 
 Plan make_plan(const oscar_cache_desc* c, int batch, int max_len, bool bf16_only) {
@@ -965,7 +965,9 @@ Plan make_plan(const oscar_cache_desc* c, int batch, int max_len, bool bf16_only
   pl.qrot_bytes = bf16_only ? 0 : static_cast<size_t>(batch) * c->num_q_heads * D * 4;
   pl.part_off = (pl.qrot_bytes + 255) & ~static_cast<size_t>(255);
   pl.part_bytes = static_cast<size_t>(batch) * c->num_q_heads * pl.n_splits * (D + 2) * 4;
-  pl.total = pl.part_off + pl.part_bytes;
+  // the rotated bf16 query of a step with rotary embedding
+  pl.qrope_off = (pl.part_off + pl.part_bytes + 255) & ~static_cast<size_t>(255);
+  pl.total = pl.qrope_off + static_cast<size_t>(batch) * c->num_q_heads * D * 2;
   return pl;
 }
 
@@ -1011,13 +1013,14 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
 
 oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, const void* k_new,
                                const void* v_new, const int32_t* seq_lens_after, int32_t batch,
-                               float* qrot, cudaStream_t st);
+                               float* qrot, double rope_log2_base, uint16_t* qrope,
+                               cudaStream_t st);
 
 oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_t* seq_lens,
                           int batch, int max_len, void* out, void* ws, size_t ws_bytes,
                           void* stream, bool bf16_only, const void* k_new = nullptr,
                           const void* v_new = nullptr, const int32_t* limits = nullptr,
-                          int rows_per_seq = 1) {
+                          int rows_per_seq = 1, double rope_log2_base = 0.0) {
   oscar_status s = oscar_host::check_desc(c, !bf16_only, true);
   if (s != OSCAR_OK) return s;
   if (batch < 0 || max_len < 1) return OSCAR_ERR_INVALID_ARG;
@@ -1068,7 +1071,13 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (k_new) {   // fused step: the append kernel writes q' and gates the split kernel
     p.after_append = 1;
-    const oscar_status a = append_with_query(c, q, k_new, v_new, seq_lens, batch, p.qrot, st);
+    uint16_t* qrope = nullptr;
+    if (rope_log2_base > 0.0) {   // the split kernel's BF16 pages take the rotated query
+      qrope = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + pl.qrope_off);
+      p.q = qrope;
+    }
+    const oscar_status a =
+        append_with_query(c, q, k_new, v_new, seq_lens, batch, p.qrot, rope_log2_base, qrope, st);
     if (a != OSCAR_OK) return a;
   }
   const bool int4 = oscar_host::code_planes(c) == 2;
@@ -1191,6 +1200,18 @@ oscar_status oscar_decode_step(const oscar_cache_desc* desc, const void* q, cons
   if (batch > 0 && (!k_new || !v_new)) return OSCAR_ERR_INVALID_ARG;
   return oscar::decode_entry(desc, q, seq_lens_after, batch, max_seq_len, out, workspace,
                              workspace_bytes, stream, false, batch > 0 ? k_new : nullptr, v_new);
+}
+
+oscar_status oscar_decode_step_rope(const oscar_cache_desc* desc, const void* q, const void* k_new,
+                                    const void* v_new, const int32_t* seq_lens_after,
+                                    int32_t batch, int32_t max_seq_len, double rope_base,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (!(rope_base > 1.0) || !std::isfinite(rope_base)) return OSCAR_ERR_INVALID_ARG;
+  if (batch > 0 && (!k_new || !v_new)) return OSCAR_ERR_INVALID_ARG;
+  return oscar::decode_entry(desc, q, seq_lens_after, batch, max_seq_len, out, workspace,
+                             workspace_bytes, stream, false, batch > 0 ? k_new : nullptr, v_new,
+                             nullptr, 1, std::log2(rope_base));
 }
 
 oscar_status oscar_decode_attention_static(const oscar_cache_desc* desc, const void* q,

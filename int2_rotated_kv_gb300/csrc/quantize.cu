@@ -54,6 +54,11 @@ struct QuantParams {
   float* qrot;           // [B][Hq][D] fp32, or null
   int hq, G;
   int planes;            // 2-bit code planes: 1 (INT2) or 2 (the INT4 variant)
+  // append only, optional: rotary position embedding of the new key and the
+  // query at the new token's position (length - 1), log2 of its base (0: none);
+  // the rotated query is also written, rounded to bf16, to qrope [B][Hq][D]
+  double rope_log2_base;
+  uint16_t* qrope;
 };
 
 template <int D>
@@ -361,6 +366,26 @@ oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------ append
+
+// cos and sin of the rotary angle m * f: the product and its reduction to
+// [-pi, pi] in fp64, then sincosf.
+__device__ __forceinline__ void rope_cs(int m, double f, float& c, float& s) {
+  double a = static_cast<double>(m) * f;
+  a -= 6.283185307179586 * rint(a * 0.15915494309189535);
+  sincosf(static_cast<float>(a), &s, &c);
+}
+
+// Rotary embedding of channel j of a head vector x (pairs j, j +- D/2), fp32,
+// rounded to bf16 (the activation precision).
+template <int D>
+__device__ __forceinline__ float rope_bf16(float xj, float xpartner, int j, int m,
+                                           const double* inv_freq) {
+  float c, s;
+  rope_cs(m, inv_freq[j % (D / 2)], c, s);
+  const float y = j < D / 2 ? __fsub_rn(__fmul_rn(xj, c), __fmul_rn(xpartner, s))
+                            : __fadd_rn(__fmul_rn(xj, c), __fmul_rn(xpartner, s));
+  return __bfloat162float(__float2bfloat16_rn(y));
+}
 //
 // One decode step's append: per sequence b, the new token goes to its BF16 slot
 // (position L-1) and, once L-1-W >= S, the token at L-1-W leaves the window: it
@@ -380,9 +405,13 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
   __shared__ __align__(16) float rs[D][32];          // R[:, 32*grp .. 32*grp + 31]
   __shared__ __align__(16) float xs[kQThreads / 32][D];
   __shared__ uint8_t cs[kQThreads / 32][32];
+  __shared__ double inv_freq[D / 2];                 // rotary base^(-2i/D)
   const int grp = blockIdx.x % NG, chunk = blockIdx.x / NG;
   const int h = blockIdx.y, kv = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool rope = p.rope_log2_base > 0.0;
+  if (rope)
+    for (int i = tid; i < D / 2; i += kQThreads) inv_freq[i] = exp2(-2.0 * i / D * p.rope_log2_base);
   // The layer's rotation is a constant of the cache and is read while the
   // predecessor grid may still run; every other input only after it has
   // completed (programmatic stream serialisation).
@@ -408,6 +437,23 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
 #pragma unroll
       for (int c = 0; c < NG; ++c) xs[warp][32 * c + lane] = bf16_to_float(qg[32 * c + lane]);
       __syncwarp();
+      if (rope) {   // the query at the new token's position, rounded to bf16
+        const int m = p.seq_lens[b] - 1;
+        float v[NG];
+#pragma unroll
+        for (int c = 0; c < NG; ++c) {
+          const int jj = 32 * c + lane;
+          v[c] = rope_bf16<D>(xs[warp][jj], xs[warp][jj < D / 2 ? jj + D / 2 : jj - D / 2], jj, m,
+                              inv_freq);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < NG; ++c) xs[warp][32 * c + lane] = v[c];
+        __syncwarp();
+        if (p.qrope)   // this CTA's 32 channels of the rotated query, for the BF16 split
+          p.qrope[(static_cast<int64_t>(b) * p.hq + h * p.G + g) * D + j] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(xs[warp][j]));
+      }
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
       for (int i = 0; i < D; i += 4) {
@@ -438,8 +484,12 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
       if (lane == 0 && grp == 0) flag(p.status, OSCAR_DEVERR_PAGE_ID);
     } else {
       const int e = kv ? 16 * D + bf16_value_elem(pn % kPage, j) : bf16_key_elem(pn % kPage, j);
-      p.bf16_pool[(static_cast<int64_t>(pg) * p.hkv + h) * (32 * D) + e] =
-          src[(static_cast<int64_t>(b) * p.hkv + h) * D + j];
+      const uint16_t* xn = src + (static_cast<int64_t>(b) * p.hkv + h) * D;
+      uint16_t val = xn[j];
+      if (rope && kv == 0)   // the new key at its position, rounded to bf16
+        val = __bfloat16_as_ushort(__float2bfloat16_rn(rope_bf16<D>(
+            bf16_to_float(val), bf16_to_float(xn[j < D / 2 ? j + D / 2 : j - D / 2]), j, pn, inv_freq)));
+      p.bf16_pool[(static_cast<int64_t>(pg) * p.hkv + h) * (32 * D) + e] = val;
     }
     // the token leaving the window
     const int po = L - 1 - p.window;
@@ -572,7 +622,8 @@ oscar_status dispatch(const QuantParams& p, int d, cudaStream_t st) {
 // CTAs also write q' = q R_K for the decode that follows.
 oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, const void* k_new,
                                const void* v_new, const int32_t* seq_lens_after, int32_t batch,
-                               float* qrot, cudaStream_t st) {
+                               float* qrot, double rope_log2_base, uint16_t* qrope,
+                               cudaStream_t st) {
   QuantParams p = base_params(desc);
   p.append = 1;
   p.n_items = batch;
@@ -582,6 +633,8 @@ oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, cons
   p.seq_lens = seq_lens_after;
   p.q = static_cast<const uint16_t*>(q);
   p.qrot = qrot;
+  p.rope_log2_base = rope_log2_base;
+  p.qrope = qrope;
   p.hq = desc->num_q_heads;
   p.G = desc->num_q_heads / desc->num_kv_heads;
   return desc->head_dim == 128 ? launch_append<128>(p, st) : launch_append<64>(p, st);

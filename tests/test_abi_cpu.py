@@ -140,6 +140,11 @@ def test_argument_errors_before_any_launch(L):
     assert lib.oscar_prefill_quantize(ctypes.byref(ok), 1, 1, 1, 1, 1, 0, 5, None) == -1
     assert lib.oscar_prefill_quantize(ctypes.byref(ok), 1, 1, 1, 1, 1, 1, 0, None) == 0
     assert lib.oscar_quantize_append(ctypes.byref(ok), None, 1, 1, 2, None) == -1
+    for base in (1.0, -3.0, float("inf"), float("nan")):     # rotary base checked first
+        assert lib.oscar_decode_step_rope(ctypes.byref(ok), 4096, 4096, 4096, 4096, 1, 16, base,
+                                          4096, 4096, 1 << 20, None) == -1
+    assert lib.oscar_decode_step_rope(ctypes.byref(ok), 4096, None, 4096, 4096, 1, 16, 1e6,
+                                      4096, 4096, 1 << 20, None) == -1
     assert lib.oscar_quantize_append(ctypes.byref(ok), 1, 1, 1, -1, None) == -1
     bf_only = _desc(L, int2_pool=None, int2_page_table=None, r_k=None, r_v=None, clip_k=None,
                     clip_v=None)
