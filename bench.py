@@ -247,7 +247,7 @@ def clone_cache(c):
 class Decoder:
     """One set of layer caches plus the per-step calls (INT2 mixed or BF16-only)."""
 
-    def __init__(self, di, rot, dev, *, bf16_only=False, l2_bytes=0, code_bits=2):
+    def __init__(self, di, rot, dev, *, bf16_only=False, l2_bytes=0, code_bits=2, rope_base=0.0):
         import torch
         from int2_rotated_kv_gb300 import _lib as L
         w = di.workload
@@ -283,6 +283,7 @@ class Decoder:
         ws = L.oscar_decode_workspace_size(base, B, self.max_len)
         self.ws = torch.empty(ws // 4 + 64, dtype=torch.float32, device=dev)
         self.n_layers = n_layers
+        self.rope_base = rope_base     # > 0: the fused step with rotary embedding
         self.launches_per_step = 3     # INT2: append+q', split, combine; BF16: append, split, combine
 
     def append(self, i, k=None, v=None, lens=None):
@@ -300,6 +301,11 @@ class Decoder:
         if self.bf16_only:
             self.append(i, k, v)
             self.attend(i, q, out=out)
+        elif self.rope_base > 0:   # the fused step with rotary embedding of q and the new key
+            c = self.caches[i % self.n_layers]
+            self.L.oscar_decode_step_rope(c, self.q if q is None else q, self.k_new if k is None else k,
+                                          self.v_new if v is None else v, self.lens_dev, self.max_len,
+                                          self.rope_base, self.out if out is None else out, self.ws)
         else:   # the library's fused step: append + attention in one call
             c = self.caches[i % self.n_layers]
             self.L.oscar_decode_step(c, self.q if q is None else q, self.k_new if k is None else k,
@@ -554,11 +560,12 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------- extras
 
-def decode_leg(di, rot, dev, l2, steps=200, warmup=10, bf16_only=False, code_bits=2):
+def decode_leg(di, rot, dev, l2, steps=200, warmup=10, bf16_only=False, code_bits=2, rope_base=0.0):
     """One layer's decode step (append + attention) at di's shape: µs, GB/s,
     and the decode call alone."""
     torch = __import__("torch")
-    dec = Decoder(di, rot, dev, bf16_only=bf16_only, l2_bytes=l2, code_bits=code_bits)
+    dec = Decoder(di, rot, dev, bf16_only=bf16_only, l2_bytes=l2, code_bits=code_bits,
+                  rope_base=rope_base)
     t, clk = time_steps(dec, steps, warmup, clocks=Clocks(torch.cuda.current_device()))
     med, mean = time_decode_calls(dec, 100)
     res = {"batch": len(di.seq_lens), "us_per_layer_step": round(t * 1e3, 3),
@@ -622,7 +629,7 @@ def extra_multiquery(dev, l2, n_calib, rows=16):
     g.manual_seed(3)
     q = torch.randn((1, rows, w.num_q_heads, w.head_dim), generator=g, device=dev).to(torch.bfloat16)
     out = torch.empty_like(q)
-    ws = torch.empty(L.oscar_decode_workspace_size(dec.caches[0], rows, Lc) // 4 + 64,
+    ws = torch.empty(L.oscar_multiquery_workspace_size(dec.caches[0], 1, rows, Lc) // 4 + 64,
                      dtype=torch.float32, device=dev)
     # the caches hold L-1 tokens until a step runs; one step fills the last slot
     for i in range(dec.n_layers):
@@ -634,8 +641,9 @@ def extra_multiquery(dev, l2, n_calib, rows=16):
     t = time_graph(dec, call, 200, 10)
     unique = attention_bytes(dec.lens, w.num_kv_heads, w.num_q_heads, w.head_dim, w.sink, w.window)
     res = {"rows": rows, "us_per_call": round(t * 1e3, 3), "rows_per_s": round(rows / (t * 1e-3), 1),
-           "unique_GBps": round(unique / t / 1e6, 1), "read_GBps": round(rows * unique / t / 1e6, 1),
-           "note": "each row reads its sequence's pages"}
+           "unique_GBps": round(unique / t / 1e6, 1),
+           "page_reads_GBps": round(rows / (8 // w.gqa) * unique / t / 1e6, 1),
+           "note": f"{8 // w.gqa} rows of the sequence share each CTA's page reads"}
     del dec
     torch.cuda.empty_cache()
     return res
@@ -715,6 +723,19 @@ def pool_bytes_per_seq(w, L, bf16_only, code_bits=2):
     d, H = w.head_dim, w.num_kv_heads
     return (pp.num_int2_pages * pages.int2_bytes_per_page(H, d, code_bits)
             + pp.num_bf16_pages * pages.bf16_bytes_per_page(H, d))
+
+
+def extra_rope(dev, l2, n_calib):
+    """The fused step with rotary position embedding (base 1e6, Qwen3) against
+    the same step without it, Qwen3-8B shape at 32768 tokens, batch 1."""
+    w = synth.QWEN3_8B_32K
+    di = synth.draw_device(w, w.seq_lens(), dev, n_calib=n_calib)
+    rot = calibrate_with_library(di, n_calib)
+    r = decode_leg(di, rot, dev, l2, rope_base=1.0e6)
+    r0 = decode_leg(di, rot, dev, l2)
+    r.pop("clocks", None)
+    r["without_rope_us_per_layer_step"] = r0["us_per_layer_step"]
+    return r
 
 
 def extra_int4(dev, l2, n_calib, budget=40e9):
@@ -834,6 +855,7 @@ EXTRA_LEGS = {
     "qwen3_8b_32k_chunk16": extra_multiquery,
     "qwen3_8b_calibration_8192": lambda dev, l2, _n: extra_calibration(dev, l2, 8192),
     "int4_variant": extra_int4,
+    "qwen3_8b_32k_rope": extra_rope,
 }
 
 

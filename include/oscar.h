@@ -209,10 +209,12 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
  *   q_pos:   int32 [batch][m_rows], device.  A position outside
  *            [0, seq_lens[b]) gives a zero output row and sets
  *            OSCAR_DEVERR_SEQ_LEN in desc->status.
- *   workspace: oscar_decode_workspace_size(desc, batch * m_rows, max_seq_len)
- *            bytes, no initial contents required.
- * Each row reads its sequence's pages (rows of one sequence do not share the
- * page reads).  Asynchronous. */
+ *   workspace: oscar_multiquery_workspace_size(desc, batch, m_rows,
+ *            max_seq_len) bytes, no initial contents required.
+ * Rows of one sequence share page reads: a CTA serves 8 / G consecutive rows
+ * of a sequence (G = num_q_heads / num_kv_heads, at most 8 per CTA), so the
+ * tensor-core tile's eight query columns carry G heads of each of those rows;
+ * G >= 8 reads the pages once per row.  Asynchronous. */
 oscar_status oscar_multiquery_attention(const oscar_cache_desc* desc, const void* q,
                                         const int32_t* seq_lens, const int32_t* q_pos,
                                         int32_t batch, int32_t m_rows, int32_t max_seq_len,
@@ -324,6 +326,12 @@ oscar_status oscar_score_covariance_device(int32_t num_kv_heads, int32_t num_q_h
 oscar_status oscar_clip_threshold_device(int32_t num_kv_heads, int32_t d, int64_t n, const void* x,
                                          const float* r, double percentile, float* clip_out,
                                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace oscar_multiquery_attention needs for `batch`
+ * sequences of m_rows query rows each (depends on the device's SM count);
+ * 0 for invalid arguments. */
+size_t oscar_multiquery_workspace_size(const oscar_cache_desc* desc, int32_t batch, int32_t m_rows,
+                                       int32_t max_seq_len);
 
 /* Number of SMs the split heuristics assume for the current device (>= 1). */
 int32_t oscar_device_sm_count(void);

@@ -26,6 +26,7 @@ EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rot
             "oscar_decode_attention", "oscar_decode_attention_bf16", "oscar_device_sm_count",
             "oscar_status_string", "oscar_version", "oscar_decode_attention_static",
             "oscar_decode_step", "oscar_decode_step_rope", "oscar_multiquery_attention",
+            "oscar_multiquery_workspace_size",
             "oscar_calibration_workspace_size", "oscar_query_covariance_device",
             "oscar_score_covariance_device", "oscar_clip_threshold_device")
 
@@ -70,6 +71,7 @@ def lib() -> ctypes.CDLL:
             "oscar_prefill_quantize": (I32, [P, P, P, P, P, P, I32, I64, P]),
             "oscar_quantize_append": (I32, [P, P, P, P, I32, P]),
             "oscar_decode_workspace_size": (ctypes.c_size_t, [P, I32, I32]),
+            "oscar_multiquery_workspace_size": (ctypes.c_size_t, [P, I32, I32, I32]),
             "oscar_decode_attention": (I32, [P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_decode_attention_bf16": (I32, [P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_device_sm_count": (I32, []),
@@ -219,6 +221,11 @@ def oscar_quantize_append(cache: Cache, k_new, v_new, seq_lens_after, stream=Non
 def oscar_decode_workspace_size(cache: Cache, batch: int, max_seq_len: int) -> int:
     d = cache.desc()
     return int(lib().oscar_decode_workspace_size(ctypes.byref(d), batch, max_seq_len))
+
+
+def oscar_multiquery_workspace_size(cache: Cache, batch: int, m_rows: int, max_seq_len: int) -> int:
+    d = cache.desc()
+    return int(lib().oscar_multiquery_workspace_size(ctypes.byref(d), batch, m_rows, max_seq_len))
 
 
 def oscar_decode_attention(cache: Cache, q, seq_lens, max_seq_len: int, out, workspace,

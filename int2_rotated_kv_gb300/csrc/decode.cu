@@ -78,6 +78,10 @@ struct DecodeParams {
   // b / rows_per_seq and sees stored tokens 0 .. limits[b] only (null: decode)
   int rows_per_seq;
   const int32_t* limits;
+  // rows of one sequence packed into the MMA tile's 8 query columns: a split
+  // CTA serves rpu consecutive rows (rpu * gq <= 8; 1 for a decode), so those
+  // rows share every page read; units = CTAs per (split, KV head slice)
+  int rpu, units;
 };
 
 // ------------------------------------------------------------------ q R_K
@@ -217,6 +221,14 @@ __device__ __forceinline__ void softmax_pair(Softmax& st, float (&la)[4], float 
   pb[0] = fast_exp2(lb[0] - b0); pb[1] = fast_exp2(lb[1] - b1);
   pb[2] = fast_exp2(lb[2] - b0); pb[3] = fast_exp2(lb[3] - b1);
 }
+
+// The query columns of one split CTA.  MMA column c (0..7) holds query head
+// qh0 + c % gq of batch row row0 + c / gq, for c < gq * nrows (the rest are
+// unused).  lim0 / lim1: the visibility limits (positions below) of this
+// thread's columns 2tig and 2tig + 1; lim_lo: the smallest over the rows.
+struct Cols {
+  int row0, nrows, qh0, lim0, lim1, lim_lo;
+};
 
 __device__ __forceinline__ bool tok_ok(int t, int L, int sink, int window, int mode, int lim) {
   // mode 0: INT2 region; 1: BF16 region (sink + recent); 2: all tokens; lim: the
@@ -380,12 +392,12 @@ __device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4],
 // w, w + 8, ... through its own ring of NS bulk-copied page-head blocks, two
 // pages per step so their dependency chains overlap and share one softmax
 // update.  Invalid page ids (negative) copy page 0 and are masked out.
-template <int D, int NS, int P>
+template <int D, int NS, int P, bool kPacked>
 __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, int lo, int n, int L, uint8_t* ring,
                                            uint64_t* bars, uint2* qbs, float (&o)[D / 16][4],
-                                           float (&zacc)[4], Softmax& sm, int defer_lp, int qh0,
-                                           int lim) {
+                                           float (&zacc)[4], Softmax& sm, int defer_lp,
+                                           const Cols& cs) {
   static_assert(NS % 2 == 0, "pages are consumed in pairs of stages");
   constexpr int NG = D / 32, NK = D / 16;
   constexpr int SB = Fmt<D, P>::kInt2Block;
@@ -419,14 +431,19 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
   uint32_t* qzs = reinterpret_cast<uint32_t*>(qbs + NK * 32);
   if (warp == 0) {
     uint32_t qz = 0;
-    const float* qr = p.qrot + (static_cast<size_t>(b) * p.hq + qh0 + gid) * D;
+    // this lane's column gid: head qh0 + gid % G of row row0 + gid / G when
+    // rows are packed, head qh0 + gid of row row0 otherwise
+    const bool cvalid = kPacked ? gid < G * cs.nrows : gid < G;
+    const int crow = kPacked && cvalid ? gid / G : 0;
+    const int chead = kPacked ? gid % G : gid;
+    const float* qr = p.qrot + (static_cast<size_t>(cs.row0 + crow) * p.hq + cs.qh0 + chead) * D;
     float gs[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) gs[g] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < NK; ++kk) {
       float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
-      if (gid < G) {
+      if (cvalid) {
         v0 = __ldcg(reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig));
         v1 = __ldcg(reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig + 8));
       }
@@ -466,7 +483,9 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     }
   }
   const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
-  const int tok_lo = p.sink, tok_hi = min(L - p.window, lim);
+  // every column sees INT2 tokens in [tok_lo, tok_hi); column 2tig (2tig+1)
+  // sees them below min(L - window, lim0 (lim1)), worked out where a page needs masking
+  const int tok_lo = p.sink, tok_hi = min(L - p.window, cs.lim_lo);
   uint32_t phase = 0;
   int s = 0;
   int i = 0;
@@ -482,10 +501,24 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     const int pA = (lo + warp + kDWarps * i) * kPage, pB = pA + kDWarps * kPage;
     if (pA < tok_lo || pB + kPage > tok_hi || (idA | idB) < 0) {
       const int t0 = pA + gid, t1 = t0 + 8, u0 = pB + gid, u1 = u0 + 8;
-      if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
-      if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
-      if (idB < 0 || u0 < tok_lo || u0 >= tok_hi) lb[0] = lb[1] = -INFINITY;
-      if (idB < 0 || u1 < tok_lo || u1 >= tok_hi) lb[2] = lb[3] = -INFINITY;
+      if constexpr (kPacked) {   // each column its own row's limit
+        const int hi0 = min(L - p.window, cs.lim0), hi1 = min(L - p.window, cs.lim1);
+        const bool a0 = idA >= 0 && t0 >= tok_lo, a1 = idA >= 0 && t1 >= tok_lo;
+        const bool c0 = idB >= 0 && u0 >= tok_lo, c1 = idB >= 0 && u1 >= tok_lo;
+        if (!(a0 && t0 < hi0)) la[0] = -INFINITY;
+        if (!(a0 && t0 < hi1)) la[1] = -INFINITY;
+        if (!(a1 && t1 < hi0)) la[2] = -INFINITY;
+        if (!(a1 && t1 < hi1)) la[3] = -INFINITY;
+        if (!(c0 && u0 < hi0)) lb[0] = -INFINITY;
+        if (!(c0 && u0 < hi1)) lb[1] = -INFINITY;
+        if (!(c1 && u1 < hi0)) lb[2] = -INFINITY;
+        if (!(c1 && u1 < hi1)) lb[3] = -INFINITY;
+      } else {
+        if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
+        if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
+        if (idB < 0 || u0 < tok_lo || u0 >= tok_hi) lb[0] = lb[1] = -INFINITY;
+        if (idB < 0 || u1 < tok_lo || u1 >= tok_hi) lb[2] = lb[3] = -INFINITY;
+      }
     }
     float pa[4], pbv[4];
     softmax_pair<NK>(sm, la, lb, o, zacc, pa, pbv);
@@ -513,8 +546,17 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     int2_qk<D, P>(stA, qbs, qz, ks, lane, la);
     const int pA = (lo + warp + kDWarps * i) * kPage;
     const int t0 = pA + gid, t1 = t0 + 8;
-    if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
-    if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
+    if constexpr (kPacked) {
+      const int hi0 = min(L - p.window, cs.lim0), hi1 = min(L - p.window, cs.lim1);
+      const bool a0 = idA >= 0 && t0 >= tok_lo, a1 = idA >= 0 && t1 >= tok_lo;
+      if (!(a0 && t0 < hi0)) la[0] = -INFINITY;
+      if (!(a0 && t0 < hi1)) la[1] = -INFINITY;
+      if (!(a1 && t1 < hi0)) la[2] = -INFINITY;
+      if (!(a1 && t1 < hi1)) la[3] = -INFINITY;
+    } else {
+      if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
+      if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
+    }
     float pa[4];
     float dummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, pd[4];
     softmax_pair<NK>(sm, la, dummy, o, zacc, pa, pd);
@@ -528,11 +570,11 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
 // so the weights are exact to ~2^-17 instead of bf16's 2^-9.  Used for the
 // sink + recent split of the mixed cache, where a query row may see only a few
 // tokens (a row early in a chunk); the all-BF16 baseline keeps one MMA.
-template <int D, int NS, bool kSplitP = false>
+template <int D, int NS, bool kSplitP, bool kPacked>
 __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, const int* lps, int n, int L, int mode,
                                            uint8_t* ring, uint64_t* bars, float (&o)[D / 16][4],
-                                           Softmax& sm, int qh0, int lim) {
+                                           Softmax& sm, const Cols& cs) {
   constexpr int NK = D / 16;
   constexpr int SB = Fmt<D>::kBf16Block;
   const int gid = lane >> 2, tig = lane & 3, G = p.gq;
@@ -557,11 +599,15 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
   if (p.after_append) prefill();
   uint32_t qb[NK][2];
   {
-    const uint16_t* qr = p.q + (static_cast<size_t>(b) * p.hq + qh0 + gid) * D;
+    // column gid: head qh0 + gid % G of row row0 + gid / G when rows are packed
+    const bool cvalid = kPacked ? gid < G * cs.nrows : gid < G;
+    const int crow = kPacked && cvalid ? gid / G : 0;
+    const int chead = kPacked ? gid % G : gid;
+    const uint16_t* qr = p.q + (static_cast<size_t>(cs.row0 + crow) * p.hq + cs.qh0 + chead) * D;
 #pragma unroll
     for (int kk = 0; kk < NK; ++kk) {
-      qb[kk][0] = gid < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig) : 0u;
-      qb[kk][1] = gid < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig + 8) : 0u;
+      qb[kk][0] = cvalid ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig) : 0u;
+      qb[kk][1] = cvalid ? *reinterpret_cast<const uint32_t*>(qr + 16 * kk + 2 * tig + 8) : 0u;
     }
   }
   const float scale_log2 = p.scale_log2;
@@ -585,8 +631,15 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
       const bool whole = mode == 2 && pbeg + kPage <= L && p.limits == nullptr;
       if (!whole) {
         const int t0 = pbeg + gid, t1 = t0 + 8;
-        if (!tok_ok(t0, L, p.sink, p.window, mode, lim)) lg[0] = lg[1] = -INFINITY;
-        if (!tok_ok(t1, L, p.sink, p.window, mode, lim)) lg[2] = lg[3] = -INFINITY;
+        if constexpr (kPacked) {   // each column its own row's limit
+          if (!tok_ok(t0, L, p.sink, p.window, mode, cs.lim0)) lg[0] = -INFINITY;
+          if (!tok_ok(t0, L, p.sink, p.window, mode, cs.lim1)) lg[1] = -INFINITY;
+          if (!tok_ok(t1, L, p.sink, p.window, mode, cs.lim0)) lg[2] = -INFINITY;
+          if (!tok_ok(t1, L, p.sink, p.window, mode, cs.lim1)) lg[3] = -INFINITY;
+        } else {
+          if (!tok_ok(t0, L, p.sink, p.window, mode, cs.lim_lo)) lg[0] = lg[1] = -INFINITY;
+          if (!tok_ok(t1, L, p.sink, p.window, mode, cs.lim_lo)) lg[2] = lg[3] = -INFINITY;
+        }
       }
       float pr[4];
       softmax_tile<NK>(sm, lg, o, zdummy, pr);
@@ -623,7 +676,9 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
   }
 }
 
-template <int D, bool kBf16Only, int P>
+// kPacked: several rows of a sequence share the CTA's query columns (multi-row
+// calls with G < 8); the decode and single-row calls use kPacked = false.
+template <int D, bool kBf16Only, int P, bool kPacked>
 __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPerSm)
     split_kernel(const DecodeParams p) {
   using C = SplitCfg<D, kBf16Only, P>;
@@ -635,7 +690,7 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBars);
   uint8_t* ring = smem + C::kRingOff;
 
-  const int split = blockIdx.x, h = blockIdx.y / p.halves, b = blockIdx.z;
+  const int split = blockIdx.x, h = blockIdx.y / p.halves, unit = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = p.gq;
@@ -650,7 +705,18 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
   const int mode = kBf16Only ? 2 : (bf16_split ? 1 : 0);
   const int first = mode == 0 ? p.sink / kPage : 0;
   const int lo = first + split * p.pps;
-  const int sb = b / p.rows_per_seq;   // the sequence this row reads
+  int sb, b, nrows;   // the sequence read, the CTA's first batch row, its rows
+  if constexpr (kPacked) {
+    const int ups = (p.rows_per_seq + p.rpu - 1) / p.rpu;   // CTA units per sequence
+    sb = unit / ups;
+    const int r_in = (unit % ups) * p.rpu;                   // first row within the sequence
+    nrows = min(p.rpu, p.rows_per_seq - r_in);
+    b = sb * p.rows_per_seq + r_in;
+  } else {
+    b = unit;
+    sb = b / p.rows_per_seq;
+    nrows = 1;
+  }
   const int32_t* pt = (mode == 0 ? p.int2_pt : p.bf16_pt) + static_cast<size_t>(sb) * p.max_pages;
   const int64_t npages = mode == 0 ? p.n_int2_pages : p.n_bf16_pages;
   int spec[(kMaxCtaPages + kDThreads - 1) / kDThreads];
@@ -666,16 +732,32 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
     if (tid == 0 && p.status) atomicOr(p.status, OSCAR_DEVERR_SEQ_LEN);
     L = 0;
   }
-  // visibility limit of this row: positions below lim (the whole cache for a decode)
-  int lim = L;
+  // visibility limits (positions below): the whole cache for a decode, per row
+  // for several rows of a sequence; lim is the widest over the CTA's rows
+  auto row_lim = [&](int r) -> int {
+    if (!p.limits) return L;
+    const int qp = p.limits[b + r];
+    return (qp < 0 || qp >= L) ? 0 : qp + 1;
+  };
+  int lim = L, lim_lo = L;
   if (p.limits) {
-    const int qp = p.limits[b];
-    if (qp < 0 || qp >= L) {
-      if (tid == 0 && p.status && L > 0) atomicOr(p.status, OSCAR_DEVERR_SEQ_LEN);
-      lim = 0;
-    } else {
-      lim = qp + 1;
+    lim = 0;
+    for (int r = 0; r < nrows; ++r) {
+      const int lr = row_lim(r);
+      if (lr == 0 && tid == 0 && p.status && L > 0) atomicOr(p.status, OSCAR_DEVERR_SEQ_LEN);
+      lim = max(lim, lr);
+      lim_lo = min(lim_lo, lr);
     }
+  }
+  Cols cs;
+  cs.row0 = b;
+  cs.nrows = nrows;
+  cs.qh0 = qh0;
+  cs.lim_lo = lim_lo;
+  cs.lim0 = cs.lim1 = lim;
+  if constexpr (kPacked) {   // this thread's columns 2tig, 2tig + 1 (unused columns: any finite limit)
+    if (2 * tig < G * nrows) cs.lim0 = row_lim((2 * tig) / G);
+    if (2 * tig + 1 < G * nrows) cs.lim1 = row_lim((2 * tig + 1) / G);
   }
   int n = 0;
   if (mode == 1) {
@@ -728,11 +810,11 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
   // the INT2 page receiving the token that leaves the window in this step
   const int defer_lp = (p.after_append && L - 1 - p.window >= p.sink) ? (L - 1 - p.window) / kPage : -1;
   if (mode == 0)
-    int2_pages<D, C::kStagesI, P>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
-                               reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp, qh0, lim);
+    int2_pages<D, C::kStagesI, P, kPacked>(p, b, h, warp, lane, ids, lo, n, L, ring, bars,
+                               reinterpret_cast<uint2*>(lps), o, zacc, sm, defer_lp, cs);
   else
-    bf16_pages<D, C::kStagesB, !kBf16Only>(p, b, h, warp, lane, ids, lps, n, L, mode, ring, bars, o, sm, qh0,
-                               lim);
+    bf16_pages<D, C::kStagesB, !kBf16Only, kPacked>(p, b, h, warp, lane, ids, lps, n, L, mode, ring,
+                                                    bars, o, sm, cs);
 
   pdl_trigger();
 
@@ -794,13 +876,14 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
     if (w == 0) gmax[g] = M;
   }
   __syncthreads();
-  for (int idx = tid; idx < G * D; idx += kDThreads) {
+  for (int idx = tid; idx < (kPacked ? G * nrows : G) * D; idx += kDThreads) {
     const int g = idx / D, ch = idx % D;
     float Os = 0.f;
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) Os = fmaf(esc[w * 8 + g], scr[w * (16 + 8 * D) + 16 + g * D + ch], Os);
     float* dst = p.part +
-                 ((static_cast<size_t>(b) * p.hq + qh0 + g) * p.n_splits + split) * (D + 2);
+                 ((static_cast<size_t>(kPacked ? b + g / G : b) * p.hq + qh0 + (kPacked ? g % G : g)) *
+                      p.n_splits + split) * (D + 2);
     if (ch == 0) {
       float Ls = 0.f;
 #pragma unroll
@@ -939,7 +1022,20 @@ struct Plan {
   size_t qrot_bytes, part_off, part_bytes, qrope_off, total;
 };
 
-Plan make_plan(const oscar_cache_desc* c, int batch, int max_len, bool bf16_only) {
+// Split-CTA units per KV head slice for `rows` batch rows of rows_per_seq rows
+// per sequence: rows of one sequence share a CTA's 8 query columns, 8 / gq of
+// them (gq = query heads per CTA); *rpu receives the rows per unit.
+int64_t split_units(const oscar_cache_desc* c, int rows, int rows_per_seq, int* rpu) {
+  const int g = c->num_q_heads / c->num_kv_heads;
+  const int gq = g < 8 ? g : 8;
+  *rpu = rows_per_seq > 1 ? std::max(1, std::min(8 / gq, rows_per_seq)) : 1;
+  return static_cast<int64_t>(rows / rows_per_seq) * ((rows_per_seq + *rpu - 1) / *rpu);
+}
+
+// n_units: split-CTA units per KV head slice (the batch rows for a decode; fewer
+// when rows of a sequence share a CTA)
+Plan make_plan(const oscar_cache_desc* c, int batch, int max_len, bool bf16_only,
+               int64_t n_units = -1) {
   Plan pl{};
   const int D = c->head_dim;
   int main_pages;
@@ -954,7 +1050,7 @@ Plan make_plan(const oscar_cache_desc* c, int batch, int max_len, bool bf16_only
   const int per_sm = bf16_only ? SplitCfg<128, true>::kCtasPerSm : SplitCfg<128, false>::kCtasPerSm;
   // one wave: units * (main splits + the BF16 split) CTAs fill every resident slot
   const int g_all = c->num_q_heads / c->num_kv_heads;
-  const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * (g_all > 8 ? g_all / 8 : 1);
+  const int64_t units = (n_units < 0 ? batch : n_units) * c->num_kv_heads * (g_all > 8 ? g_all / 8 : 1);
   const int64_t slots = static_cast<int64_t>(per_sm) * oscar_host::sm_count();
   int n_main = static_cast<int>(std::max<int64_t>(1, slots / units - (bf16_only ? 0 : 1)));
   n_main = std::min(n_main, main_pages);
@@ -987,12 +1083,13 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int D, bool kBf16Only, int P>
+template <int D, bool kBf16Only, int P, bool kPacked = false>
 oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) {
   using C = SplitCfg<D, kBf16Only, P>;
-  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(split_kernel<D, kBf16Only, P>), C::kBytes))
+  if (!oscar_host::allow_smem(reinterpret_cast<const void*>(split_kernel<D, kBf16Only, P, kPacked>),
+                              C::kBytes))
     return OSCAR_ERR_CUDA;
-  const dim3 sgrid(pl.n_splits, p.hkv * p.halves, p.batch);
+  const dim3 sgrid(pl.n_splits, p.hkv * p.halves, p.units);
   cudaError_t e;
   // every kernel is launched with programmatic stream serialisation: it may
   // start while its predecessor drains, and waits (griddepcontrol.wait) before
@@ -1002,9 +1099,9 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
       e = launch_pdl(qrot_kernel<D>, dim3(p.hkv * p.halves, p.batch), dim3(1024), 0, st, p);
       if (e != cudaSuccess) return OSCAR_ERR_CUDA;
     }
-    e = launch_pdl(split_kernel<D, kBf16Only, P>, sgrid, dim3(kDThreads), C::kBytes, st, p);
+    e = launch_pdl(split_kernel<D, kBf16Only, P, kPacked>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   } else {
-    e = launch_pdl(split_kernel<D, kBf16Only, P>, sgrid, dim3(kDThreads), C::kBytes, st, p);
+    e = launch_pdl(split_kernel<D, kBf16Only, P, kPacked>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   }
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   e = launch_pdl(combine_kernel<D, kBf16Only>, dim3(p.G, p.hkv, p.batch), dim3(256), 0, st, p);
@@ -1033,7 +1130,9 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   if (!bf16_only &&
       (c->sink + kPage - 1) / kPage + (c->window + kPage - 1) / kPage + 1 > kMaxCtaPages)
     return OSCAR_ERR_UNSUPPORTED;
-  const Plan pl = make_plan(c, batch, max_len, bf16_only);
+  int rpu = 1;
+  const int64_t n_units = split_units(c, batch, rows_per_seq, &rpu);
+  const Plan pl = make_plan(c, batch, max_len, bf16_only, n_units);
   if (pl.n_splits > kMaxSplits) return OSCAR_ERR_UNSUPPORTED;
   if (ws_bytes < pl.total) return OSCAR_ERR_WORKSPACE;
   DecodeParams p{};
@@ -1059,6 +1158,8 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.seq_lens = seq_lens;
   p.batch = batch;   // rows: sequences x rows_per_seq
   p.rows_per_seq = rows_per_seq;
+  p.rpu = rpu;
+  p.units = static_cast<int>(n_units);
   p.limits = limits;
   p.max_len = max_len;
   p.n_main = pl.n_main;
@@ -1081,11 +1182,16 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
     if (a != OSCAR_OK) return a;
   }
   const bool int4 = oscar_host::code_planes(c) == 2;
+  const bool packed = rpu > 1;
   if (c->head_dim == 128) {
     if (bf16_only) return run_decode<128, true, 1>(p, pl, st);
+    if (packed)
+      return int4 ? run_decode<128, false, 2, true>(p, pl, st) : run_decode<128, false, 1, true>(p, pl, st);
     return int4 ? run_decode<128, false, 2>(p, pl, st) : run_decode<128, false, 1>(p, pl, st);
   }
   if (bf16_only) return run_decode<64, true, 1>(p, pl, st);
+  if (packed)
+    return int4 ? run_decode<64, false, 2, true>(p, pl, st) : run_decode<64, false, 1, true>(p, pl, st);
   return int4 ? run_decode<64, false, 2>(p, pl, st) : run_decode<64, false, 1>(p, pl, st);
 }
 
@@ -1181,6 +1287,16 @@ oscar_status oscar_decode_attention_bf16(const oscar_cache_desc* desc, const voi
 }
 
 int32_t oscar_device_sm_count(void) { return oscar_host::sm_count(); }
+
+size_t oscar_multiquery_workspace_size(const oscar_cache_desc* desc, int32_t batch, int32_t m_rows,
+                                       int32_t max_seq_len) {
+  if (oscar_host::check_desc(desc, false, false) != OSCAR_OK || batch < 1 || m_rows < 1 ||
+      max_seq_len < 1 || static_cast<int64_t>(batch) * m_rows > (int64_t(1) << 30))
+    return 0;
+  int rpu = 1;
+  const int64_t units = oscar::split_units(desc, batch * m_rows, m_rows, &rpu);
+  return oscar::make_plan(desc, batch * m_rows, max_seq_len, false, units).total;
+}
 
 oscar_status oscar_multiquery_attention(const oscar_cache_desc* desc, const void* q,
                                         const int32_t* seq_lens, const int32_t* q_pos,
