@@ -434,11 +434,11 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
     for (int task = warp; task < n_seq * p.G; task += kQThreads / 32) {
       const int b = chunk * kAppendSeqs + task / p.G, g = task % p.G;
       const uint16_t* qg = p.q + (static_cast<int64_t>(b) * p.hq + h * p.G + g) * D;
+      const int m = rope ? p.seq_lens[b] - 1 : 0;   // issued with the query loads, not after them
 #pragma unroll
       for (int c = 0; c < NG; ++c) xs[warp][32 * c + lane] = bf16_to_float(qg[32 * c + lane]);
       __syncwarp();
       if (rope) {   // the query at the new token's position, rounded to bf16
-        const int m = p.seq_lens[b] - 1;
         float v[NG];
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
