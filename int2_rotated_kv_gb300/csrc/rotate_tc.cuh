@@ -315,28 +315,46 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
         break;
       }
       int* mi = meta + s * 2 * kTcM;
+      // The four tokens of each lane are resolved level by level, so each level's
+      // loads are in flight together: ids and positions, then the sequences'
+      // lengths, then the page-table entries (three round trips per tile).
+      constexpr int U = kTcM / 32;
+      int seq[U], pos[U], L[U], pg[U];
+      bool ok2[U];
 #pragma unroll
-      for (int u = 0; u < kTcM / 32; ++u) {
+      for (int u = 0; u < U; ++u) {
+        const int64_t item = tile * kTcM + u * 32 + lane;
+        const bool in = item < p.n_items;
+        seq[u] = in ? p.seq_ids[item] : -1;
+        pos[u] = in ? p.positions[item] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        L[u] = (seq[u] >= 0 && seq[u] < p.num_seqs) ? p.seq_lens[seq[u]] : -1;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        ok2[u] = seq[u] >= 0 && seq[u] < p.num_seqs && pos[u] >= 0 && pos[u] < L[u] &&
+                 pos[u] / kPage < p.max_pages;
+        pg[u] = -1;
+        if (ok2[u]) {
+          const int64_t trow = static_cast<int64_t>(seq[u]) * p.max_pages + pos[u] / kPage;
+          pg[u] = (pos[u] >= p.sink && pos[u] < L[u] - p.window) ? p.int2_pt[trow] : p.bf16_pt[trow];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
         const int row = u * 32 + lane;
         const int64_t item = tile * kTcM + row;
         int i2 = -1, bf = -1;
         if (item < p.n_items) {
-          const int seq = p.seq_ids[item];
-          const int pos = p.positions[item];
-          const int L = (seq >= 0 && seq < p.num_seqs) ? p.seq_lens[seq] : -1;
-          if (seq < 0 || seq >= p.num_seqs || pos < 0 || pos >= L || pos / kPage >= p.max_pages) {
+          if (!ok2[u]) {
             flag(p.status, OSCAR_DEVERR_SEQ_LEN);
+          } else if (pos[u] >= p.sink && pos[u] < L[u] - p.window) {
+            if (pg[u] < 0 || pg[u] >= p.n_int2_pages) flag(p.status, OSCAR_DEVERR_PAGE_ID);
+            else i2 = pg[u] * kPage + pos[u] % kPage;
           } else {
-            const int64_t trow = static_cast<int64_t>(seq) * p.max_pages + pos / kPage;
-            if (pos >= p.sink && pos < L - p.window) {
-              const int pg = p.int2_pt[trow];
-              if (pg < 0 || pg >= p.n_int2_pages) flag(p.status, OSCAR_DEVERR_PAGE_ID);
-              else i2 = pg * kPage + pos % kPage;
-            } else {
-              const int pg = p.bf16_pt[trow];
-              if (pg < 0 || pg >= p.n_bf16_pages) flag(p.status, OSCAR_DEVERR_PAGE_ID);
-              else bf = pg * kPage + pos % kPage;
-            }
+            if (pg[u] < 0 || pg[u] >= p.n_bf16_pages) flag(p.status, OSCAR_DEVERR_PAGE_ID);
+            else bf = pg[u] * kPage + pos[u] % kPage;
           }
         }
         mi[row] = i2;
