@@ -431,53 +431,54 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       const float sf = __half2float(s16), zf = __half2float(z16);
       const bool live = sf != 0.f;            // a zero scale gives code 0 everywhere
       const float inv = live ? __fdiv_rn(1.0f, sf) : 0.f;
-      auto code = [&](int j) -> uint32_t {
-        return live ? static_cast<uint32_t>(tc_code(y[j], zf, sf, inv, kMaxCode)) : 0u;
-      };
       const uint32_t sz = static_cast<uint32_t>(__half_as_ushort(s16)) |
                           (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
-      // each code is decided once; plane 0 takes its highest two bits
+      uint32_t bytes[P][8];
+#pragma unroll
+      for (int pl = 0; pl < P; ++pl)
+#pragma unroll
+        for (int b8 = 0; b8 < 8; ++b8) bytes[pl][b8] = 0u;
+      uint32_t near = 0u;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float a = __fsub_rn(y[j], zf);
+        const float q = __fmul_rn(a, inv);
+        const float r = rintf(q);
+        near |= (fabsf(fabsf(q - r) - 0.5f) < 4e-6f * (1.f + fabsf(q)) ? 1u : 0u) << j;
+        const uint32_t c = static_cast<uint32_t>(min(max(static_cast<int>(r), 0), kMaxCode));
+        const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
+#pragma unroll
+        for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
+      }
+      if (live && near != 0u) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if ((near >> j) & 1u) {
+            const float a = __fsub_rn(y[j], zf);
+            const uint32_t c =
+                static_cast<uint32_t>(min(max(static_cast<int>(rintf(__fdiv_rn(a, sf))), 0), kMaxCode));
+            const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
+#pragma unroll
+            for (int pl = 0; pl < P; ++pl)
+              bytes[pl][j & 7] = (bytes[pl][j & 7] & ~(3u << pos)) |
+                                 (((c >> (2 * (P - 1 - pl))) & 3u) << pos);
+          }
+        }
+      }
       if (kv == 0) {
 #pragma unroll
-        for (int tig = 0; tig < 4; ++tig)
+        for (int b8 = 0; b8 < 8; ++b8)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            uint32_t c4[4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-              for (int i = 0; i < 2; ++i) c4[2 * hh + i] = code(16 * i + 8 * hh + 2 * tig + e);
-#pragma unroll
-            for (int pl = 0; pl < P; ++pl) {
-              const int shift = 2 * (P - 1 - pl);
-              uint32_t byte = 0;
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int i = 0; i < 2; ++i) byte |= ((c4[2 * hh + i] >> shift) & 3u) << (4 * hh + 2 * i);
-              blk[F::kKc + pl * F::kPlane + key_byte<D>(slot, tig, grp, e)] = static_cast<uint8_t>(byte);
-            }
-          }
+          for (int pl = 0; pl < P; ++pl)
+            blk[F::kKc + pl * F::kPlane + key_byte<D>(slot, b8 >> 1, grp, b8 & 1)] =
+                static_cast<uint8_t>(bytes[pl][b8]);
         reinterpret_cast<uint32_t*>(blk + F::kKsz)[slot * NG + grp] = sz;
       } else {
 #pragma unroll
-        for (int gid = 0; gid < 8; ++gid) {
-          uint32_t c4[4];
+        for (int b8 = 0; b8 < 8; ++b8)
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-            for (int i = 0; i < 2; ++i) c4[2 * ch + i] = code(16 * i + 8 * ch + gid);
-#pragma unroll
-          for (int pl = 0; pl < P; ++pl) {
-            const int shift = 2 * (P - 1 - pl);
-            uint32_t byte = 0;
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-              for (int i = 0; i < 2; ++i) byte |= ((c4[2 * ch + i] >> shift) & 3u) << (4 * ch + 2 * i);
-            blk[F::kVc + pl * F::kPlane + value_byte<D>(slot, gid, grp)] = static_cast<uint8_t>(byte);
-          }
-        }
+          for (int pl = 0; pl < P; ++pl)
+            blk[F::kVc + pl * F::kPlane + value_byte<D>(slot, b8, grp)] = static_cast<uint8_t>(bytes[pl][b8]);
         const int e = vsz_index<D>(slot, grp);
         reinterpret_cast<uint16_t*>(blk + F::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
         reinterpret_cast<uint16_t*>(blk + F::kVz)[e] = static_cast<uint16_t>(sz >> 16);
