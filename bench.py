@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--n-calib", type=int, default=None)
     ap.add_argument("--profile", action="store_true",
                     help="minimal run for ncu: one layer cache, eager steps, no extra legs")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --profile: this many sequences of the workload's context, drawn on the device")
     ap.add_argument("--code-bits", type=int, default=2, choices=[2, 4],
                     help="with --profile: the INT4 variant's caches (the headline is INT2)")
     ap.add_argument("--leg", default=None, choices=sorted(EXTRA_LEGS),
@@ -894,7 +896,11 @@ def main():
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     if args.profile:
         # launches in order: 1 prefill, then per step the fused append (+ q'), split, combine
-        dec = Decoder(device_inputs(inst, dev), rot, dev, l2_bytes=0, code_bits=args.code_bits)
+        if args.batch:   # a large batch: inputs drawn on the device, the same recipe
+            di = synth.draw_device(w, np.full(args.batch, int(w.seq_lens().max())), dev, n_calib=n_calib)
+        else:
+            di = device_inputs(inst, dev)
+        dec = Decoder(di, rot, dev, l2_bytes=0, code_bits=args.code_bits)
         for i in range(args.warmup + args.steps):
             dec.step(i)
         torch.cuda.synchronize()

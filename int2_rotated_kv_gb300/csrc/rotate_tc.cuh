@@ -438,31 +438,31 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       for (int pl = 0; pl < P; ++pl)
 #pragma unroll
         for (int b8 = 0; b8 < 8; ++b8) bytes[pl][b8] = 0u;
-      uint32_t near = 0u;
+      // q is within ~2 ulp (< 4e-6 for q < 16) of the correctly rounded quotient
+      bool near = false;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float a = __fsub_rn(y[j], zf);
         const float q = __fmul_rn(a, inv);
         const float r = rintf(q);
-        near |= (fabsf(fabsf(q - r) - 0.5f) < 4e-6f * (1.f + fabsf(q)) ? 1u : 0u) << j;
+        near |= fabsf(fabsf(q - r) - 0.5f) < 6.4e-5f;
         const uint32_t c = static_cast<uint32_t>(min(max(static_cast<int>(r), 0), kMaxCode));
         const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
 #pragma unroll
         for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
       }
-      if (live && near != 0u) {
+      if (live && near) {   // rare: the whole group again with the correctly rounded division
+#pragma unroll
+        for (int pl = 0; pl < P; ++pl)
+#pragma unroll
+          for (int b8 = 0; b8 < 8; ++b8) bytes[pl][b8] = 0u;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          if ((near >> j) & 1u) {
-            const float a = __fsub_rn(y[j], zf);
-            const uint32_t c =
-                static_cast<uint32_t>(min(max(static_cast<int>(rintf(__fdiv_rn(a, sf))), 0), kMaxCode));
-            const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
+          const uint32_t c = static_cast<uint32_t>(
+              min(max(static_cast<int>(rintf(__fdiv_rn(__fsub_rn(y[j], zf), sf))), 0), kMaxCode));
+          const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
 #pragma unroll
-            for (int pl = 0; pl < P; ++pl)
-              bytes[pl][j & 7] = (bytes[pl][j & 7] & ~(3u << pos)) |
-                                 (((c >> (2 * (P - 1 - pl))) & 3u) << pos);
-          }
+          for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
         }
       }
       if (kv == 0) {
