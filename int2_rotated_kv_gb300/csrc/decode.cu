@@ -272,36 +272,42 @@ __device__ __forceinline__ void load_words(const uint8_t* base, int lane, uint32
   }
 }
 
-// q.K for one code page-head.  P = 2 (INT4 variant): the code is 4 * hi + lo,
-// each plane read as INT2 codes; the high plane's dot products weigh 4.
-template <int D, int P>
-__device__ __forceinline__ void int2_qk(const uint8_t* st, const uint2* qbs, uint32_t qz, float ks,
-                                        int lane, float (&lg)[4]) {
+// q.K for NPG code page-heads at once (one or two: the query operand is read
+// once for both).  P = 2 (INT4 variant): the code is 4 * hi + lo, each plane
+// read as INT2 codes; the high plane's dot products weigh 4.  Each group's dot
+// products are weighed by the token's key scale, and the sum is brought to
+// log2-domain logits by one multiply-add onto the zero term.
+template <int D, int P, int NPG>
+__device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const uint2* qbs,
+                                        uint32_t qz, float ks, int lane, float (&lg)[NPG][4]) {
   using F = Fmt<D, P>;
   constexpr int NG = D / 32;
   const int gid = lane >> 2, tig = lane & 3;
-  uint32_t kw[P][NG];
+  uint32_t kw[NPG][P][NG], sa[NPG][NG], sb[NPG][NG];
+  float zt[NPG][4], acc[NPG][4];
 #pragma unroll
-  for (int pl = 0; pl < P; ++pl) load_words<NG>(st + F::kKc + pl * F::kPlane, lane, kw[pl]);
-  const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + F::kKsz);
-  uint32_t za = 0, zb = 0;
-  if (tig < NG) {
-    const uint32_t e0 = ksz[gid * NG + tig], e1 = ksz[(gid + 8) * NG + tig];
-    za = __byte_perm(e0, e0, 0x3232);
-    zb = __byte_perm(e1, e1, 0x3232);
-  }
-  mma_f16_z(lg, za, zb, 0u, 0u, qz, 0u);          // zero term, already in log2 units
-  uint32_t sa[NG], sb[NG];
-  if constexpr (NG == 4) {
-    const uint4 a = reinterpret_cast<const uint4*>(ksz)[gid];
-    const uint4 c = reinterpret_cast<const uint4*>(ksz)[gid + 8];
-    sa[0] = a.x; sa[1] = a.y; sa[2] = a.z; sa[3] = a.w;
-    sb[0] = c.x; sb[1] = c.y; sb[2] = c.z; sb[3] = c.w;
-  } else {
-    const uint2 a = reinterpret_cast<const uint2*>(ksz)[gid];
-    const uint2 c = reinterpret_cast<const uint2*>(ksz)[gid + 8];
-    sa[0] = a.x; sa[1] = a.y;
-    sb[0] = c.x; sb[1] = c.y;
+  for (int pg = 0; pg < NPG; ++pg) {
+#pragma unroll
+    for (int pl = 0; pl < P; ++pl) load_words<NG>(st[pg] + F::kKc + pl * F::kPlane, lane, kw[pg][pl]);
+    const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st[pg] + F::kKsz);
+    uint32_t za = 0, zb = 0;
+    if (tig < NG) {
+      const uint32_t e0 = ksz[gid * NG + tig], e1 = ksz[(gid + 8) * NG + tig];
+      za = __byte_perm(e0, e0, 0x3232);
+      zb = __byte_perm(e1, e1, 0x3232);
+    }
+    mma_f16_z(zt[pg], za, zb, 0u, 0u, qz, 0u);     // zero term, already in log2 units
+    if constexpr (NG == 4) {
+      const uint4 a = reinterpret_cast<const uint4*>(ksz)[gid];
+      const uint4 c = reinterpret_cast<const uint4*>(ksz)[gid + 8];
+      sa[pg][0] = a.x; sa[pg][1] = a.y; sa[pg][2] = a.z; sa[pg][3] = a.w;
+      sb[pg][0] = c.x; sb[pg][1] = c.y; sb[pg][2] = c.z; sb[pg][3] = c.w;
+    } else {
+      const uint2 a = reinterpret_cast<const uint2*>(ksz)[gid];
+      const uint2 c = reinterpret_cast<const uint2*>(ksz)[gid + 8];
+      sa[pg][0] = a.x; sa[pg][1] = a.y;
+      sb[pg][0] = c.x; sb[pg][1] = c.y;
+    }
   }
 #pragma unroll
   for (int m = 0; m < NG; ++m) {
@@ -309,26 +315,38 @@ __device__ __forceinline__ void int2_qk(const uint8_t* st, const uint2* qbs, uin
     // by 8, so every extracted half is code * 4^i * 16^(s&1) * 2^-24
     const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
     const uint2 b0 = qbs[(2 * m) * 32 + lane], b1 = qbs[(2 * m + 1) * 32 + lane];
-    float dg[4];
-    {   // A registers a0..a3 hold key pairs s = 0, 2, 1, 3 (lowest plane)
-      const uint32_t wl = kw[P - 1][m], wh = kw[P - 1][m] >> 8;
-      mma_f16_z(dg, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
-      mma_f16(dg, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
-    }
-    if constexpr (P == 2) {   // high plane: code bits 3..2
-      const uint32_t wl = kw[0][m], wh = kw[0][m] >> 8;
-      float dh[4];
-      mma_f16_z(dh, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
-      mma_f16(dh, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) dg[k] = fmaf(4.f, dh[k], dg[k]);
+    for (int pg = 0; pg < NPG; ++pg) {
+      float dg[4];
+      {   // A registers a0..a3 hold key pairs s = 0, 2, 1, 3 (lowest plane)
+        const uint32_t wl = kw[pg][P - 1][m], wh = kw[pg][P - 1][m] >> 8;
+        mma_f16_z(dg, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
+        mma_f16(dg, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+      }
+      if constexpr (P == 2) {   // high plane: code bits 3..2
+        const uint32_t wl = kw[pg][0][m], wh = kw[pg][0][m] >> 8;
+        float dh[4];
+        mma_f16_z(dh, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
+        mma_f16(dh, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dg[k] = fmaf(4.f, dh[k], dg[k]);
+      }
+      const float fa = half_lo(sa[pg][m]), fb = half_lo(sb[pg][m]);
+      if (m == 0) {
+        acc[pg][0] = fa * dg[0]; acc[pg][1] = fa * dg[1];
+        acc[pg][2] = fb * dg[2]; acc[pg][3] = fb * dg[3];
+      } else {
+        acc[pg][0] = fmaf(fa, dg[0], acc[pg][0]);
+        acc[pg][1] = fmaf(fa, dg[1], acc[pg][1]);
+        acc[pg][2] = fmaf(fb, dg[2], acc[pg][2]);
+        acc[pg][3] = fmaf(fb, dg[3], acc[pg][3]);
+      }
     }
-    const float fa = half_lo(sa[m]) * ks, fb = half_lo(sb[m]) * ks;
-    lg[0] = fmaf(fa, dg[0], lg[0]);
-    lg[1] = fmaf(fa, dg[1], lg[1]);
-    lg[2] = fmaf(fb, dg[2], lg[2]);
-    lg[3] = fmaf(fb, dg[3], lg[3]);
   }
+#pragma unroll
+  for (int pg = 0; pg < NPG; ++pg)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) lg[pg][k] = fmaf(acc[pg][k], ks, zt[pg][k]);
 }
 
 // p.V for one INT2 page-head: o (channel x query head) += codes^T (p * s), plus
@@ -495,9 +513,13 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     if (!wait_stage<NS, true>(wbar, s + 1, phase, i + 1, my_n, ids, warp, p.status)) return;
     const uint8_t* stA = wring + s * SB;
     const uint8_t* stB = stA + SB;
-    float la[4], lb[4];
-    int2_qk<D, P>(stA, qbs, qz, ks, lane, la);
-    int2_qk<D, P>(stB, qbs, qz, ks, lane, lb);
+    float lab[2][4];
+    {
+      const uint8_t* const sts[2] = {stA, stB};
+      int2_qk<D, P, 2>(sts, qbs, qz, ks, lane, lab);
+    }
+    float (&la)[4] = lab[0];
+    float (&lb)[4] = lab[1];
     const int pA = (lo + warp + kDWarps * i) * kPage, pB = pA + kDWarps * kPage;
     if (pA < tok_lo || pB + kPage > tok_hi || (idA | idB) < 0) {
       const int t0 = pA + gid, t1 = t0 + 8, u0 = pB + gid, u1 = u0 + 8;
@@ -542,8 +564,12 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     const int idA = wids[kDWarps * i];
     if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
     const uint8_t* stA = wring + s * SB;
-    float la[4];
-    int2_qk<D, P>(stA, qbs, qz, ks, lane, la);
+    float l1[1][4];
+    {
+      const uint8_t* const sts[1] = {stA};
+      int2_qk<D, P, 1>(sts, qbs, qz, ks, lane, l1);
+    }
+    float (&la)[4] = l1[0];
     const int pA = (lo + warp + kDWarps * i) * kPage;
     const int t0 = pA + gid, t1 = t0 + 8;
     if constexpr (kPacked) {
