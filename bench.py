@@ -415,23 +415,21 @@ def time_decode_calls(dec, iters=200, batch=40):
 
 
 def time_e2e(dec, steps, warmup):
-    """Through the C ABI with host buffers: per step copy q and the new K/V from
-    pinned host memory, append + attend, copy the output back."""
-    torch = dec.torch
-    hq = torch.empty(dec.q.shape, dtype=torch.bfloat16).pin_memory()
-    hk = torch.empty(dec.k_new.shape, dtype=torch.bfloat16).pin_memory()
-    hv = torch.empty(dec.v_new.shape, dtype=torch.bfloat16).pin_memory()
-    hq.copy_(dec.q.cpu()); hk.copy_(dec.k_new.cpu()); hv.copy_(dec.v_new.cpu())
+    """Through the C ABI with host buffers (oscar_decode_step_host): every step
+    the library copies q and the new K/V in from one pinned host buffer, runs
+    the fused step, and copies the output back to pinned host memory."""
+    torch, L = dec.torch, dec.L
+    assert not dec.bf16_only
+    hin = torch.cat([dec.q.reshape(-1), dec.k_new.reshape(-1),
+                     dec.v_new.reshape(-1)]).cpu().pin_memory()
     ho = torch.empty(dec.out.shape, dtype=torch.bfloat16).pin_memory()
-    dq, dk, dv, do = (torch.empty_like(dec.q), torch.empty_like(dec.k_new),
-                      torch.empty_like(dec.v_new), torch.empty_like(dec.out))
+    B = int(dec.lens_dev.numel())
+    staging = torch.empty(L.oscar_decode_step_host_staging_size(dec.caches[0], B) // 4 + 4,
+                          dtype=torch.float32, device=dec.dev)
 
     def one(i):
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dec.step(i, dq, dk, dv, do)
-        ho.copy_(do, non_blocking=True)
+        L.oscar_decode_step_host(dec.caches[i % dec.n_layers], hin, dec.lens_dev, dec.max_len, ho,
+                                 staging, dec.ws, rope_base=dec.rope_base)
 
     for i in range(warmup):
         one(i)
@@ -442,8 +440,7 @@ def time_e2e(dec, steps, warmup):
         one(i)
     e1.record()
     torch.cuda.synchronize()
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
-    return e0.elapsed_time(e1) / steps, h2d, ho.numel() * 2
+    return e0.elapsed_time(e1) / steps, hin.numel() * 2, ho.numel() * 2
 
 
 # -------------------------------------------------------------- CPU / oracle

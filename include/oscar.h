@@ -256,6 +256,44 @@ oscar_status oscar_decode_step_rope(const oscar_cache_desc* desc, const void* q,
                                     void* out, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/* Bytes of device staging that oscar_decode_step_host needs for `batch`
+ * sequences: the step's inputs (see below), then, from the next multiple of
+ * 256 bytes, the device copy of the output.  0 for an invalid descriptor or
+ * batch < 1. */
+size_t oscar_decode_step_host_staging_size(const oscar_cache_desc* desc, int32_t batch);
+
+/* The fused decode step (oscar_decode_step, or oscar_decode_step_rope when
+ * rope_base > 0) for a caller whose step tensors live in host memory, as in a
+ * serving loop that receives the new token's projections from the host.
+ *   in_host: host, contiguous bf16, in this order: q [batch][Hq][d], k_new
+ *     [batch][Hkv][d], v_new [batch][Hkv][d]
+ *     (oscar_decode_step_host_staging_size's input part, batch*(Hq+2Hkv)*d*2 bytes).
+ *   out_host: host, bf16 [batch][Hq][d], written when the stream reaches the end
+ *     of the call.
+ *   staging: device, 16-byte aligned, staging_bytes >=
+ *     oscar_decode_step_host_staging_size(desc, batch).
+ *   seq_lens_after, workspace, max_seq_len: as oscar_decode_step (device).
+ * When both host buffers are page-locked memory mapped into the device's
+ * address space (cudaHostAlloc memory under unified addressing, or
+ * cudaHostRegister'ed with mapping; each range's first and last bytes are
+ * checked with cudaPointerGetAttributes), the step's kernels read q, k_new and
+ * v_new from in_host and write the output to out_host in place, over the
+ * CPU-GPU link.  Otherwise one host-to-device copy of in_host into staging
+ * precedes the kernels and one device-to-host copy of the output follows them
+ * (asynchronous only for page-locked memory).  Everything is queued on
+ * `stream`; the call returns once the work is queued: synchronise the stream
+ * before reading out_host or reusing in_host.  Every argument is checked
+ * before anything is queued: OSCAR_ERR_INVALID_ARG for a null or misaligned
+ * buffer or rope_base < 0, OSCAR_ERR_WORKSPACE for staging or workspace that is
+ * too small, then oscar_decode_step's errors; OSCAR_ERR_CUDA when a copy cannot
+ * be queued.  Result: the bytes oscar_decode_step writes to its `out` and the
+ * cache, with the same inputs. */
+oscar_status oscar_decode_step_host(const oscar_cache_desc* desc, const void* in_host,
+                                    const int32_t* seq_lens_after, int32_t batch,
+                                    int32_t max_seq_len, double rope_base, void* out_host,
+                                    void* staging, size_t staging_bytes, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
 /* oscar_decode_attention for callers that cannot allocate device memory.
  * The pages describe no counterpart; it exists because some callers have no
  * allocator at hand when they run attention: a plug-in inside a runtime that

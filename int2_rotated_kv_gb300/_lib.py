@@ -26,7 +26,8 @@ EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rot
             "oscar_decode_attention", "oscar_decode_attention_bf16", "oscar_device_sm_count",
             "oscar_status_string", "oscar_version", "oscar_decode_attention_static",
             "oscar_decode_step", "oscar_decode_step_rope", "oscar_multiquery_attention",
-            "oscar_multiquery_workspace_size",
+            "oscar_multiquery_workspace_size", "oscar_decode_step_host_staging_size",
+            "oscar_decode_step_host",
             "oscar_calibration_workspace_size", "oscar_query_covariance_device",
             "oscar_score_covariance_device", "oscar_clip_threshold_device")
 
@@ -78,6 +79,9 @@ def lib() -> ctypes.CDLL:
             "oscar_decode_attention_static": (I32, [P, P, P, I32, I32, P, P]),
             "oscar_decode_step": (I32, [P, P, P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_decode_step_rope": (I32, [P, P, P, P, P, I32, I32, D, P, P, ctypes.c_size_t, P]),
+            "oscar_decode_step_host_staging_size": (ctypes.c_size_t, [P, I32]),
+            "oscar_decode_step_host": (I32, [P, P, P, I32, I32, D, P, P, ctypes.c_size_t, P,
+                                             ctypes.c_size_t, P]),
             "oscar_multiquery_attention": (I32, [P, P, P, P, I32, I32, I32, P, P, ctypes.c_size_t, P]),
             "oscar_calibration_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I64]),
             "oscar_query_covariance_device": (I32, [I32, I32, I32, I64, P, P, P, ctypes.c_size_t, P]),
@@ -271,6 +275,29 @@ def oscar_decode_step_rope(cache: Cache, q, k_new, v_new, seq_lens_after, max_se
                                         _ptr(seq_lens_after), int(seq_lens_after.numel()),
                                         int(max_seq_len), float(rope_base), _ptr(out),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
+
+
+def oscar_decode_step_host_staging_size(cache: Cache, batch: int) -> int:
+    """Device staging bytes of oscar_decode_step_host for `batch` sequences."""
+    return int(lib().oscar_decode_step_host_staging_size(ctypes.byref(cache.desc()), int(batch)))
+
+
+def oscar_decode_step_host(cache: Cache, in_host, seq_lens_after, max_seq_len: int, out_host,
+                           staging, workspace, rope_base: float = 0.0, stream=None):
+    """The fused decode step with its inputs and result in host memory.
+
+    in_host: host bf16 tensor holding q [B][Hq][d], k_new [B][Hkv][d] and
+    v_new [B][Hkv][d] back to back (pinned for asynchronous copies); out_host:
+    host bf16 [B][Hq][d]; staging, workspace: device bytes.  Everything is
+    queued on the stream; synchronise it before reading out_host."""
+    d = cache.desc()
+    _check("oscar_decode_step_host",
+           lib().oscar_decode_step_host(ctypes.byref(d), _ptr(in_host), _ptr(seq_lens_after),
+                                        int(seq_lens_after.numel()), int(max_seq_len),
+                                        float(rope_base), _ptr(out_host), _ptr(staging),
+                                        staging.numel() * staging.element_size(), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
 
 

@@ -1139,11 +1139,24 @@ oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, cons
                                float* qrot, double rope_log2_base, uint16_t* qrope,
                                cudaStream_t st);
 
+// Host buffers of a step whose inputs and result live in host memory: the
+// inputs are copied in after every check has passed and before the first
+// kernel, the result is copied out after the last, on the call's stream.
+struct HostCopy {
+  void* in_dst;
+  const void* in_src;
+  size_t in_bytes;
+  void* out_dst;
+  const void* out_src;
+  size_t out_bytes;
+};
+
 oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_t* seq_lens,
                           int batch, int max_len, void* out, void* ws, size_t ws_bytes,
                           void* stream, bool bf16_only, const void* k_new = nullptr,
                           const void* v_new = nullptr, const int32_t* limits = nullptr,
-                          int rows_per_seq = 1, double rope_log2_base = 0.0) {
+                          int rows_per_seq = 1, double rope_log2_base = 0.0,
+                          const HostCopy* hc = nullptr) {
   oscar_status s = oscar_host::check_desc(c, !bf16_only, true);
   if (s != OSCAR_OK) return s;
   if (batch < 0 || max_len < 1) return OSCAR_ERR_INVALID_ARG;
@@ -1196,6 +1209,9 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->head_dim)));
   p.wait_first = bf16_only ? 1 : 0;   // the INT2 call is gated by qrot_kernel
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (hc && cudaMemcpyAsync(hc->in_dst, hc->in_src, hc->in_bytes, cudaMemcpyHostToDevice, st) !=
+                cudaSuccess)
+    return OSCAR_ERR_CUDA;
   if (k_new) {   // fused step: the append kernel writes q' and gates the split kernel
     p.after_append = 1;
     uint16_t* qrope = nullptr;
@@ -1209,16 +1225,43 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   }
   const bool int4 = oscar_host::code_planes(c) == 2;
   const bool packed = rpu > 1;
+  oscar_status r;
   if (c->head_dim == 128) {
-    if (bf16_only) return run_decode<128, true, 1>(p, pl, st);
-    if (packed)
-      return int4 ? run_decode<128, false, 2, true>(p, pl, st) : run_decode<128, false, 1, true>(p, pl, st);
-    return int4 ? run_decode<128, false, 2>(p, pl, st) : run_decode<128, false, 1>(p, pl, st);
+    if (bf16_only) r = run_decode<128, true, 1>(p, pl, st);
+    else if (packed)
+      r = int4 ? run_decode<128, false, 2, true>(p, pl, st) : run_decode<128, false, 1, true>(p, pl, st);
+    else
+      r = int4 ? run_decode<128, false, 2>(p, pl, st) : run_decode<128, false, 1>(p, pl, st);
+  } else {
+    if (bf16_only) r = run_decode<64, true, 1>(p, pl, st);
+    else if (packed)
+      r = int4 ? run_decode<64, false, 2, true>(p, pl, st) : run_decode<64, false, 1, true>(p, pl, st);
+    else
+      r = int4 ? run_decode<64, false, 2>(p, pl, st) : run_decode<64, false, 1>(p, pl, st);
   }
-  if (bf16_only) return run_decode<64, true, 1>(p, pl, st);
-  if (packed)
-    return int4 ? run_decode<64, false, 2, true>(p, pl, st) : run_decode<64, false, 1, true>(p, pl, st);
-  return int4 ? run_decode<64, false, 2>(p, pl, st) : run_decode<64, false, 1>(p, pl, st);
+  if (r == OSCAR_OK && hc &&
+      cudaMemcpyAsync(hc->out_dst, hc->out_src, hc->out_bytes, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  return r;
+}
+
+// Staging of a step with host buffers: the inputs (q, k_new, v_new, in the
+// caller's host order) from byte 0, the output from the next multiple of 256.
+struct HostStaging {
+  size_t q_bytes, kv_bytes, in_bytes, out_off, out_bytes, total;
+};
+
+inline HostStaging host_staging(const oscar_cache_desc* c, int batch) {
+  HostStaging h{};
+  const size_t b = static_cast<size_t>(batch), d = static_cast<size_t>(c->head_dim);
+  h.q_bytes = b * c->num_q_heads * d * 2;
+  h.kv_bytes = b * c->num_kv_heads * d * 2;
+  h.in_bytes = h.q_bytes + 2 * h.kv_bytes;
+  h.out_off = (h.in_bytes + 255) / 256 * 256;
+  h.out_bytes = h.q_bytes;
+  h.total = h.out_off + h.out_bytes;
+  return h;
 }
 
 }  // namespace oscar
@@ -1235,6 +1278,28 @@ int sm_count() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
   cached[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+// The device address of host range [p, p + bytes) when it is page-locked memory
+// mapped into the device's address space (cudaHostAlloc memory under unified
+// addressing, or cudaHostRegister'ed with mapping) and its first and last bytes
+// map to one contiguous device range; null otherwise (a query error is cleared).
+const void* mapped_range(const void* p, size_t bytes) {
+  if (!p || bytes == 0) return nullptr;
+  cudaPointerAttributes a{}, b{};
+  const uint8_t* last = static_cast<const uint8_t*>(p) + (bytes - 1);
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess ||
+      cudaPointerGetAttributes(&b, last) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || b.type != cudaMemoryTypeHost || !a.devicePointer ||
+      !b.devicePointer)
+    return nullptr;
+  if (static_cast<const uint8_t*>(b.devicePointer) !=
+      static_cast<const uint8_t*>(a.devicePointer) + (bytes - 1))
+    return nullptr;
+  return a.devicePointer;
 }
 
 bool allow_smem(const void* func, int bytes) {
@@ -1354,6 +1419,45 @@ oscar_status oscar_decode_step_rope(const oscar_cache_desc* desc, const void* q,
   return oscar::decode_entry(desc, q, seq_lens_after, batch, max_seq_len, out, workspace,
                              workspace_bytes, stream, false, batch > 0 ? k_new : nullptr, v_new,
                              nullptr, 1, std::log2(rope_base));
+}
+
+size_t oscar_decode_step_host_staging_size(const oscar_cache_desc* desc, int32_t batch) {
+  if (oscar_host::check_desc(desc, false, false) != OSCAR_OK || batch < 1) return 0;
+  return oscar::host_staging(desc, batch).total;
+}
+
+oscar_status oscar_decode_step_host(const oscar_cache_desc* desc, const void* in_host,
+                                    const int32_t* seq_lens_after, int32_t batch,
+                                    int32_t max_seq_len, double rope_base, void* out_host,
+                                    void* staging, size_t staging_bytes, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  oscar_status st = oscar_host::check_desc(desc, true, true);
+  if (st != OSCAR_OK) return st;
+  if (batch < 0 || max_seq_len < 1) return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return OSCAR_OK;
+  if (!(rope_base >= 0.0) || !std::isfinite(rope_base) || (rope_base > 0.0 && !(rope_base > 1.0)))
+    return OSCAR_ERR_INVALID_ARG;
+  if (!in_host || !out_host || !staging) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(staging) & 15) return OSCAR_ERR_INVALID_ARG;
+  const oscar::HostStaging h = oscar::host_staging(desc, batch);
+  if (staging_bytes < h.total) return OSCAR_ERR_WORKSPACE;
+  const double lb = rope_base > 0.0 ? std::log2(rope_base) : 0.0;
+  // Page-locked host buffers mapped into the device's address space are read
+  // and written by the kernels in place (over the CPU-GPU link, no copy-engine
+  // hop); any other host memory goes through the staging copies.
+  const uint8_t* in_dev = static_cast<const uint8_t*>(oscar_host::mapped_range(in_host, h.in_bytes));
+  uint8_t* out_dev =
+      static_cast<uint8_t*>(const_cast<void*>(oscar_host::mapped_range(out_host, h.out_bytes)));
+  uint8_t* sg = static_cast<uint8_t*>(staging);
+  if (in_dev && out_dev && (reinterpret_cast<uintptr_t>(in_dev) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(out_dev) & 3) == 0)
+    return oscar::decode_entry(desc, in_dev, seq_lens_after, batch, max_seq_len, out_dev,
+                               workspace, workspace_bytes, stream, false, in_dev + h.q_bytes,
+                               in_dev + h.q_bytes + h.kv_bytes, nullptr, 1, lb);
+  const oscar::HostCopy hc{sg, in_host, h.in_bytes, out_host, sg + h.out_off, h.out_bytes};
+  return oscar::decode_entry(desc, sg, seq_lens_after, batch, max_seq_len, sg + h.out_off,
+                             workspace, workspace_bytes, stream, false, sg + h.q_bytes,
+                             sg + h.q_bytes + h.kv_bytes, nullptr, 1, lb, &hc);
 }
 
 oscar_status oscar_decode_attention_static(const oscar_cache_desc* desc, const void* q,

@@ -153,6 +153,42 @@ def test_argument_errors_before_any_launch(L):
                                            None) == -3   # reaches the workspace check
 
 
+def test_host_step_staging_and_argument_errors_before_any_copy(L):
+    """oscar_decode_step_host: staging = inputs (q, k_new, v_new back to back),
+    then the output from the next multiple of 256 bytes; every argument is
+    checked before the first copy is queued."""
+    lib = L.lib()
+    ok = _desc(L)                                    # Hkv 1, Hq 4, d 64
+    # batch 3: q 3*4*64*2 = 1536 B, k and v 384 B each: inputs 2304 B (a multiple
+    # of 256), output 1536 B from there
+    assert lib.oscar_decode_step_host_staging_size(ctypes.byref(ok), 3) == 2304 + 1536
+    g1 = _desc(L, num_q_heads=1)                     # inputs 384 B -> output from 512
+    assert lib.oscar_decode_step_host_staging_size(ctypes.byref(g1), 1) == 512 + 128
+    assert lib.oscar_decode_step_host_staging_size(ctypes.byref(ok), 0) == 0
+    assert lib.oscar_decode_step_host_staging_size(None, 1) == 0
+    need = lib.oscar_decode_step_host_staging_size(ctypes.byref(ok), 1)
+
+    def call(in_host=4096, batch=1, max_len=16, rope=0.0, out_host=8192, staging=1 << 16,
+             staging_bytes=need, ws_bytes=1 << 20, desc=ok):
+        return lib.oscar_decode_step_host(ctypes.byref(desc) if desc is not None else None,
+                                          in_host, 4096, batch, max_len, rope, out_host, staging,
+                                          staging_bytes, 1 << 20, ws_bytes, None)
+
+    assert call(desc=None) == -1
+    assert call(in_host=None) == -1
+    assert call(out_host=None) == -1
+    assert call(staging=None) == -1
+    assert call(staging=(1 << 16) + 8) == -1          # staging not 16-byte aligned
+    assert call(staging_bytes=need - 1) == -3
+    for rope in (0.5, 1.0, -1.0, float("inf"), float("nan")):
+        assert call(rope=rope) == -1, rope
+    assert call(max_len=0) == -1
+    assert call(batch=-1) == -1
+    assert call(ws_bytes=8) == -3                     # the decode step's own workspace check
+    assert call(batch=0) == 0
+    assert call(desc=_desc(L, head_dim=96)) == -2
+
+
 def test_calibration_argument_errors_before_any_launch(L):
     lib = L.lib()
     ws = lambda *a: lib.oscar_calibration_workspace_size(*a)
