@@ -431,7 +431,11 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
     // computing channel 32*grp + j
     const int64_t left = p.n_items - static_cast<int64_t>(chunk) * kAppendSeqs;
     const int n_seq = static_cast<int>(left < kAppendSeqs ? left : kAppendSeqs);
-    for (int task = warp; task < n_seq * p.G; task += kQThreads / 32) {
+    // task t runs on warp (t + n_seq) mod 8: warps 0 .. n_seq-1 also place a
+    // token each below, so with few sequences the two chains run side by side
+    constexpr int kWarps = kQThreads / 32;
+    const int t0 = ((warp - n_seq) % kWarps + kWarps) % kWarps;
+    for (int task = t0; task < n_seq * p.G; task += kWarps) {
       const int b = chunk * kAppendSeqs + task / p.G, g = task % p.G;
       const uint16_t* qg = p.q + (static_cast<int64_t>(b) * p.hq + h * p.G + g) * D;
       const int m = rope ? p.seq_lens[b] - 1 : 0;   // issued with the query loads, not after them
