@@ -475,31 +475,34 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
   for (int u = warp; u < kAppendSeqs; u += kQThreads / 32) {
     const int b = chunk * kAppendSeqs + u;
     if (b >= p.n_items) break;
+    // loads are issued level by level: the length with the new token's values,
+    // then every page-table entry the length selects, then the pages
     const int L = p.seq_lens[b];
+    const uint16_t* xn = src + (static_cast<int64_t>(b) * p.hkv + h) * D;
+    const uint16_t xv = xn[j];
+    const uint16_t xr = (rope && kv == 0) ? xn[j < D / 2 ? j + D / 2 : j - D / 2] : 0;
     if (L < 1 || (L - 1) / kPage >= p.max_pages) {
       if (lane == 0 && grp == 0) flag(p.status, OSCAR_DEVERR_SEQ_LEN);
       continue;
     }
     const int64_t base = static_cast<int64_t>(b) * p.max_pages;
-    // the new token's channel j -> its BF16 slot
-    const int pn = L - 1;
+    const int pn = L - 1;                 // the new token -> its BF16 slot
+    const int po = L - 1 - p.window;      // the token leaving the window
+    const bool leaves = po >= p.sink;
     const int pg = p.bf16_pt[base + pn / kPage];
+    const int sp = leaves ? p.bf16_pt[base + po / kPage] : -1;
+    const int dp = leaves ? p.int2_pt[base + po / kPage] : -1;
     if (pg < 0 || pg >= p.n_bf16_pages) {
       if (lane == 0 && grp == 0) flag(p.status, OSCAR_DEVERR_PAGE_ID);
     } else {
       const int e = kv ? 16 * D + bf16_value_elem(pn % kPage, j) : bf16_key_elem(pn % kPage, j);
-      const uint16_t* xn = src + (static_cast<int64_t>(b) * p.hkv + h) * D;
-      uint16_t val = xn[j];
+      uint16_t val = xv;
       if (rope && kv == 0)   // the new key at its position, rounded to bf16
         val = __bfloat16_as_ushort(__float2bfloat16_rn(rope_bf16<D>(
-            bf16_to_float(val), bf16_to_float(xn[j < D / 2 ? j + D / 2 : j - D / 2]), j, pn, inv_freq)));
+            bf16_to_float(xv), bf16_to_float(xr), j, pn, inv_freq)));
       p.bf16_pool[(static_cast<int64_t>(pg) * p.hkv + h) * (32 * D) + e] = val;
     }
-    // the token leaving the window
-    const int po = L - 1 - p.window;
-    if (po < p.sink) continue;
-    const int sp = p.bf16_pt[base + po / kPage];
-    const int dp = p.int2_pt[base + po / kPage];
+    if (!leaves) continue;
     if (sp < 0 || sp >= p.n_bf16_pages || dp < 0 || dp >= p.n_int2_pages) {
       if (lane == 0 && grp == 0) flag(p.status, OSCAR_DEVERR_PAGE_ID);
       continue;
