@@ -22,9 +22,10 @@
 //              d) and, from one lane, issues 3 * d/16 MMAs (M = 128 tokens,
 //              N = d, K = 16) per tile; tcgen05.commit frees the ring stage and
 //              publishes the accumulator;
-//   warp 2     destinations: each token's INT2 or BF16 slot (sequence, length
-//              and page-table lookups) for tiles ahead, into a shared ring;
-//   warps 3..  epilogue, d/32 warpgroups: a warp reads TMEM lanes 32*(w%4) ..
+//   warps 2, 3 destinations, alternate tiles: each token's INT2 or BF16 slot
+//              (sequence, length and page-table lookups) for tiles ahead, into
+//              a shared ring (one warp alone needed most of a tile's time);
+//   warps 4..  epilogue, d/32 warpgroups: a warp reads TMEM lanes 32*(w%4) ..
 //              +31 (one token per thread) and one group of 32 columns, then in
 //              the thread's own registers: clip, min/max, s16, z16, codes, and
 //              the stores into the page format (each byte of the format holds
@@ -56,7 +57,7 @@ struct TcSmem {
   static constexpr int kMisc = kBars + 24 * 8;              // u32 tmem base, int abort, int issued, int mma_done
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kEpiWarps = 4 * (D / 32);            // one warp per (lane quarter, group)
-  static constexpr int kThreads = 32 * (3 + kEpiWarps);
+  static constexpr int kThreads = 32 * (4 + kEpiWarps);
   static constexpr int kAlloc = kBytes + 1024;              // the base is rounded up to 1024 bytes
   static constexpr int kCols = 2 * D;                       // TMEM columns: two accumulators
   static_assert(kA % 1024 == 0 && kStage % 1024 == 0 && kPiece % 1024 == 0,
@@ -302,11 +303,12 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
         *n_mma = it + 1;
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 || warp == 3) {
     // -------------------------------------------------------- destinations
     // per row: INT2 slot (page * 16 + slot) or -1, BF16 slot likewise
-    int it = 0;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    int it = warp - 2;   // this warp's tiles: every second one of the CTA's
+    for (int64_t tile = blockIdx.x + static_cast<int64_t>(warp - 2) * gridDim.x; tile < n_tiles;
+         tile += 2 * static_cast<int64_t>(gridDim.x), it += 2) {
       const int s = it % kTcMeta;
       const uint32_t ph = static_cast<uint32_t>(it / kTcMeta) & 1u;
       const bool ok = !*abort_flag && mbar_wait(&meta_empty[s], ph ^ 1u, p.status);
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;             // TMEM lanes this warp may read
-    const int grp = (warp - 3) >> 2;          // its group of 32 columns
+    const int grp = (warp - 4) >> 2;          // its group of 32 columns
     const int row = 32 * quarter + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     const float clip = (kv ? p.clip_v : p.clip_k)[h];
@@ -419,18 +421,25 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       using F = Fmt<D, P>;
       constexpr int kMaxCode = P == 2 ? 15 : 3;   // INT4 variant / INT2
       uint8_t* blk = p.int2_pool + (static_cast<int64_t>(i2 / kPage) * p.hkv + h) * F::kInt2Block;
-      float mn = INFINITY, mx = -INFINITY;
+      // Clipping is monotone, so the clipped group's minimum and maximum are
+      // the clipped extremes of the raw values, and a value beyond the clip
+      // threshold lands on code 0 or the top code either way: the values
+      // themselves are never clipped on this path.
+      float mn = y[0], mx = y[0];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        y[j] = fminf(fmaxf(y[j], -clip), clip);
+      for (int j = 1; j < 32; ++j) {
         mn = fminf(mn, y[j]);
         mx = fmaxf(mx, y[j]);
       }
+      mn = fminf(fmaxf(mn, -clip), clip);
+      mx = fminf(fmaxf(mx, -clip), clip);
       const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kMaxCode)));
       const __half z16 = __float2half_rn(mn);
       const float sf = __half2float(s16), zf = __half2float(z16);
       const bool live = sf != 0.f;            // a zero scale gives code 0 everywhere
-      const float inv = live ? __fdiv_rn(1.0f, sf) : 0.f;
+      // approximate reciprocal (a few ulp): the quotient stays far inside the
+      // near-tie margin below of the correctly rounded one
+      const float inv = live ? __fdividef(1.0f, sf) : 0.f;
       const uint32_t sz = static_cast<uint32_t>(__half_as_ushort(s16)) |
                           (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
       uint32_t bytes[P][8];
@@ -438,15 +447,20 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       for (int pl = 0; pl < P; ++pl)
 #pragma unroll
         for (int b8 = 0; b8 < 8; ++b8) bytes[pl][b8] = 0u;
-      // q is within ~2 ulp (< 4e-6 for q < 16) of the correctly rounded quotient
+      // code = round-half-even of the quotient clamped to [0, top] (the same as
+      // clamping the rounded quotient): adding 1.5 * 2^23 rounds it to an
+      // integer held in the low mantissa bits.  A clamped quotient within
+      // 6.4e-5 of a half-integer flags the group for the correctly rounded
+      // division; at the clamp bounds both roundings give the same code.
+      constexpr float kMagic = 12582912.0f;
       bool near = false;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float a = __fsub_rn(y[j], zf);
-        const float q = __fmul_rn(a, inv);
-        const float r = rintf(q);
-        near |= fabsf(fabsf(q - r) - 0.5f) < 6.4e-5f;
-        const uint32_t c = static_cast<uint32_t>(min(max(static_cast<int>(r), 0), kMaxCode));
+        const float qc = fminf(fmaxf(__fmul_rn(__fsub_rn(y[j], zf), inv), 0.f),
+                               static_cast<float>(kMaxCode));
+        const float m = __fadd_rn(qc, kMagic);
+        near |= fabsf(__fsub_rn(qc, __fsub_rn(m, kMagic))) > 0.5f - 6.4e-5f;
+        const uint32_t c = __float_as_uint(m);
         const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
 #pragma unroll
         for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
@@ -458,8 +472,9 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
           for (int b8 = 0; b8 < 8; ++b8) bytes[pl][b8] = 0u;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
+          const float yc = fminf(fmaxf(y[j], -clip), clip);
           const uint32_t c = static_cast<uint32_t>(
-              min(max(static_cast<int>(rintf(__fdiv_rn(__fsub_rn(y[j], zf), sf))), 0), kMaxCode));
+              min(max(static_cast<int>(rintf(__fdiv_rn(__fsub_rn(yc, zf), sf))), 0), kMaxCode));
           const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
 #pragma unroll
           for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
