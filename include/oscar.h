@@ -284,7 +284,8 @@ size_t oscar_decode_step_host_staging_size(const oscar_cache_desc* desc, int32_t
  * `stream`; the call returns once the work is queued: synchronise the stream
  * before reading out_host or reusing in_host.  Every argument is checked
  * before anything is queued: OSCAR_ERR_INVALID_ARG for a null or misaligned
- * buffer or rope_base < 0, OSCAR_ERR_WORKSPACE for staging or workspace that is
+ * buffer or a rope_base that is neither 0 (no rotary embedding) nor finite and
+ * > 1, OSCAR_ERR_WORKSPACE for staging or workspace that is
  * too small, then oscar_decode_step's errors; OSCAR_ERR_CUDA when a copy cannot
  * be queued.  Result: the bytes oscar_decode_step writes to its `out` and the
  * cache, with the same inputs. */
