@@ -98,8 +98,23 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def gpu_id(index):
+    """The nvidia-smi identifier of torch device `index`: its UUID, so that a
+    remapped CUDA_VISIBLE_DEVICES still names the GPU this process runs on (the
+    torch index and the nvidia-smi index differ under remapping)."""
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(index).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    return str(index)
+
+
 class Clocks:
-    """nvidia-smi sampler running while the timed region runs."""
+    """nvidia-smi sampler running while the timed region runs; `gpu` is an
+    nvidia-smi device identifier (UUID preferred, see gpu_id)."""
 
     FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -152,7 +167,8 @@ class Clocks:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(rows), "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
+                "samples": len(rows), "power_w_max": max((num(r[4]) or 0.0) for r in rows),
+                "gpu": self.gpu}
 
 
 def kernel_source_hash():
@@ -339,6 +355,10 @@ def time_steps(dec, steps, warmup, chunk=64, clocks=None, barrier=None):
     g_rem = dec.graph(0, rem) if rem else None
     for i in range(warmup):
         dec.step(i)
+    # the first replay of a graph uploads it to the device: done here, untimed
+    g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
     torch.cuda.synchronize()
     if barrier:
         barrier()
@@ -565,7 +585,7 @@ def decode_leg(di, rot, dev, l2, steps=200, warmup=10, bf16_only=False, code_bit
     torch = __import__("torch")
     dec = Decoder(di, rot, dev, bf16_only=bf16_only, l2_bytes=l2, code_bits=code_bits,
                   rope_base=rope_base)
-    t, clk = time_steps(dec, steps, warmup, clocks=Clocks(torch.cuda.current_device()))
+    t, clk = time_steps(dec, steps, warmup, clocks=Clocks(gpu_id(torch.cuda.current_device())))
     med, mean = time_decode_calls(dec, 100)
     res = {"batch": len(di.seq_lens), "us_per_layer_step": round(t * 1e3, 3),
            "GBps": round(dec.step_bytes / t / 1e6, 1), "decode_call_us": round(med * 1e3, 3),
@@ -908,7 +928,7 @@ def main():
         return
     di = device_inputs(inst, dev)
     dec = Decoder(di, rot, dev, l2_bytes=l2)
-    clocks = Clocks(local)
+    clocks = Clocks(gpu_id(local))
     ms, clk = time_steps(dec, args.steps, args.warmup, clocks=clocks, barrier=barrier)
     ms_all = max_over_ranks(ms, world, dev)
     value = job_gbps(dec.step_bytes, ms_all, world)

@@ -1151,24 +1151,36 @@ struct HostCopy {
   size_t out_bytes;
 };
 
-oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_t* seq_lens,
-                          int batch, int max_len, void* out, void* ws, size_t ws_bytes,
-                          void* stream, bool bf16_only, const void* k_new = nullptr,
-                          const void* v_new = nullptr, const int32_t* limits = nullptr,
-                          int rows_per_seq = 1, double rope_log2_base = 0.0,
-                          const HostCopy* hc = nullptr) {
+// Argument checks of every decode entry point, in the order the callers rely
+// on: descriptor, sizes, pointers and alignment, then the shape limits.  A
+// batch of 0 passes (the caller returns OSCAR_OK without launching).
+// with_ws: the caller passes a workspace pointer, checked too.
+oscar_status decode_args(const oscar_cache_desc* c, const void* q, const int32_t* seq_lens,
+                         int batch, int max_len, const void* out, const void* ws, bool bf16_only,
+                         bool with_ws = true) {
   oscar_status s = oscar_host::check_desc(c, !bf16_only, true);
   if (s != OSCAR_OK) return s;
   if (batch < 0 || max_len < 1) return OSCAR_ERR_INVALID_ARG;
   if (batch == 0) return OSCAR_OK;
-  if (!q || !seq_lens || !out || !ws) return OSCAR_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(ws) & 15) return OSCAR_ERR_INVALID_ARG;
+  if (!q || !seq_lens || !out) return OSCAR_ERR_INVALID_ARG;
+  if (with_ws && (!ws || (reinterpret_cast<uintptr_t>(ws) & 15))) return OSCAR_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 3)
     return OSCAR_ERR_INVALID_ARG;
   if (max_len > static_cast<int64_t>(c->max_pages_per_seq) * kPage) return OSCAR_ERR_INVALID_ARG;
   if (!bf16_only &&
       (c->sink + kPage - 1) / kPage + (c->window + kPage - 1) / kPage + 1 > kMaxCtaPages)
     return OSCAR_ERR_UNSUPPORTED;
+  return OSCAR_OK;
+}
+
+oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_t* seq_lens,
+                          int batch, int max_len, void* out, void* ws, size_t ws_bytes,
+                          void* stream, bool bf16_only, const void* k_new = nullptr,
+                          const void* v_new = nullptr, const int32_t* limits = nullptr,
+                          int rows_per_seq = 1, double rope_log2_base = 0.0,
+                          const HostCopy* hc = nullptr) {
+  oscar_status s = decode_args(c, q, seq_lens, batch, max_len, out, ws, bf16_only);
+  if (s != OSCAR_OK || batch == 0) return s;
   int rpu = 1;
   const int64_t n_units = split_units(c, batch, rows_per_seq, &rpu);
   const Plan pl = make_plan(c, batch, max_len, bf16_only, n_units);
@@ -1332,20 +1344,49 @@ namespace oscar {
 
 constexpr size_t kStaticScratchBytes = sizeof(g_decode_scratch);
 
-// Device address of the scratch buffer on the current device.  In host code the
-// symbol is only a handle; cudaGetSymbolAddress, called once per device with
-// that device current, yields the address the kernels are given.
+// The current CUDA context's unique id (cuCtxGetId through the runtime's driver
+// entry points, so the library does not link the driver library); 0 when it
+// cannot be had.  Ids are never reused, unlike context handles.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrent)(CUcontext*);
+  typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+  static const std::pair<GetCurrent, GetId> fns = [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa{}, qb{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) !=
+            cudaSuccess || qa != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+            cudaSuccess || qb != cudaDriverEntryPointSuccess)
+      return std::make_pair(static_cast<GetCurrent>(nullptr), static_cast<GetId>(nullptr));
+    return std::make_pair(reinterpret_cast<GetCurrent>(a), reinterpret_cast<GetId>(b));
+  }();
+  if (!fns.first || !fns.second) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (fns.first(&ctx) != CUDA_SUCCESS || !ctx || fns.second(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch buffer in the current device's context.  In
+// host code the symbol is only a handle; cudaGetSymbolAddress, called with the
+// device current, yields the address the kernels are given.  It is looked up
+// once per context: a context that was destroyed and created again (after
+// cudaDeviceReset, say) reloads the library's module, so the address is looked
+// up afresh rather than taken from a cache keyed on the device index alone.
 void* decode_scratch_address() {
   static std::mutex mu;
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return nullptr;
-    addr[dev] = ptr;
-  }
+  const unsigned long long ctx = current_context_id();
+  if (addr[dev] && ctx != 0 && ctx_of[dev] == ctx) return addr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return nullptr;
+  addr[dev] = ptr;
+  ctx_of[dev] = current_context_id();   // the lookup has made the context current
   return addr[dev];
 }
 
@@ -1463,10 +1504,11 @@ oscar_status oscar_decode_step_host(const oscar_cache_desc* desc, const void* in
 oscar_status oscar_decode_attention_static(const oscar_cache_desc* desc, const void* q,
                                            const int32_t* seq_lens, int32_t batch,
                                            int32_t max_seq_len, void* out, void* stream) {
-  oscar_status st = oscar_host::check_desc(desc, true, true);
-  if (st != OSCAR_OK) return st;
-  if (batch < 0 || max_seq_len < 1) return OSCAR_ERR_INVALID_ARG;
-  if (batch == 0) return OSCAR_OK;
+  // the workspace call's argument checks first (the scratch stands in for the
+  // workspace pointer), so an invalid argument is reported as such
+  oscar_status st = oscar::decode_args(desc, q, seq_lens, batch, max_seq_len, out, nullptr, false,
+                                       false);
+  if (st != OSCAR_OK || batch == 0) return st;
   // the same plan the workspace call makes; refuse it if it needs more scratch
   const oscar::Plan pl = oscar::make_plan(desc, batch, max_seq_len, false);
   if (pl.total > oscar::kStaticScratchBytes) return OSCAR_ERR_WORKSPACE;

@@ -108,7 +108,6 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
   const int kv = blockIdx.z;      // 0 keys, 1 values
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* rot = (kv ? p.r_v : p.r_k) + static_cast<size_t>(h) * D * D;
-  const float clip = (kv ? p.clip_v : p.clip_k)[h];
   const uint16_t* src = kv ? p.v_src : p.k_src;
 
   // the head's rotation arrives in shared memory by one bulk copy
@@ -118,9 +117,11 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
     fence_mbar_init();
   }
   // launched with programmatic stream serialisation: inputs are read only after
-  // the predecessor grid has completed; then the next kernel may launch
+  // the predecessor grid has completed (the clip too: a calibration kernel just
+  // before this one may have written it); then the next kernel may launch
   pdl_wait();
   pdl_trigger();
+  const float clip = (kv ? p.clip_v : p.clip_k)[h];
   __syncthreads();
   if (tid == 0) {
     mbar_arrive_expect_tx(bar, D * D * 4);
@@ -222,7 +223,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
     if (!need_rot) continue;
     if (!r_ready) {
       r_ready = __syncthreads_and(mbar_wait(bar, 0, p.status));
-      if (!r_ready) return;   // recorded as a timeout; nothing usable to rotate with
+      // recorded as a timeout; nothing usable to rotate with.  The copy may
+      // still be in flight, so the CTA leaves through the bounded wait below.
+      if (!r_ready) break;
     }
     __syncthreads();
 

@@ -135,7 +135,7 @@ def decode(cache, q, lens, max_len=None, bf16_only=False, out=None):
 
 
 def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=None, upto=None,
-                         heads=None):
+                         heads=None, seqs=None):
     """The oracle's attention over what the GPU actually stored: every token of
     every sequence read back from the pools (INT2 codes, s16, z16 dequantised and
     rotated back with R^T; BF16 tokens as stored), then fp64 softmax attention.
@@ -144,7 +144,8 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=Non
     optional {sequence: logical pages} whose tokens are left out.  ``upto``:
     optional last visible position per sequence (a query row of a chunk).  The
     code width (INT2 or the INT4 variant) is the cache's ``code_bits``.
-    ``heads``: optional KV heads to compute (the others' outputs stay zero)."""
+    ``heads``: optional KV heads to compute (the others' outputs stay zero).
+    ``seqs``: optional sequences to compute (likewise)."""
     got2, gotb = pools(cache)
     B, Hq, d = q.shape
     hkv = Hq // gqa
@@ -152,7 +153,7 @@ def attention_from_pools(cache, pp, q, lens, rot, *, sink, window, gqa, drop=Non
     blk2 = layout.int2_block_bytes(d, bits)
     blkb = layout.bf16_block_bytes(d) // 2
     out = np.zeros((B, Hq, d))
-    for b in range(B):
+    for b in (range(B) if seqs is None else seqs):
         L = int(lens[b])
         t = np.arange(L)
         m = ocache.is_int2(t, L, sink, window)

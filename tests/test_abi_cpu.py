@@ -151,6 +151,16 @@ def test_argument_errors_before_any_launch(L):
     assert lib.oscar_quantize_append(ctypes.byref(bf_only), 1, 1, 1, 2, None) == -1
     assert lib.oscar_decode_attention_bf16(ctypes.byref(bf_only), 4096, 4096, 1, 16, 4096, 4096, 8,
                                            None) == -3   # reaches the workspace check
+    # the no-allocation entry point checks its arguments as the workspace call
+    # does, before it sizes the plan against its fixed scratch buffer
+    st = lib.oscar_decode_attention_static
+    assert st(ctypes.byref(ok), 4096, 4096, 1, 10 ** 6, 4096, None) == -1   # beyond the page table
+    assert st(ctypes.byref(ok), None, 4096, 1, 16, 4096, None) == -1
+    assert st(ctypes.byref(ok), 4096, None, 1, 16, 4096, None) == -1
+    assert st(ctypes.byref(ok), 4096, 4096, 1, 16, 4098, None) == -1       # misaligned output
+    assert st(ctypes.byref(ok), 4096, 4096, -1, 16, 4096, None) == -1
+    assert st(ctypes.byref(ok), 4096, 4096, 0, 16, 4096, None) == 0
+    assert st(ctypes.byref(_desc(L, head_dim=96)), 4096, 4096, 1, 16, 4096, None) == -2
 
 
 def test_host_step_staging_and_argument_errors_before_any_copy(L):
