@@ -48,7 +48,11 @@
  *     values, 16*d bf16 each, same fragment order).
  * Stored INT2 values are, per group of 32 rotated channels, code*s + z with
  * s = fp16((max-min)/3), z = fp16(min) of the clipped group and
- * code = round-half-even((y_clipped - z)/s) in [0, 3] (0 when s == 0).
+ * code = round-half-even((y_clipped - z)/s) in [0, 3] (0 when s == 0).  A
+ * group whose rotated values are not all finite (a NaN or an infinity in the
+ * token's input makes every rotated value non-finite) is stored as a zero group,
+ * s = z = 0 and codes 0, and OSCAR_DEVERR_NONFINITE is set.  BF16 tokens are
+ * stored as given, NaN included.
  *
  * INT4 variant (desc->code_bits = 4; a format beside the pages' INT2, for the
  * comparison with INT4 caches in [Summary 4]): sixteen levels, s = fp16((max -
@@ -80,6 +84,9 @@ typedef int oscar_status;
 #define OSCAR_DEVERR_PAGE_ID 1       /* a page id outside [0, num_pages) was skipped    */
 #define OSCAR_DEVERR_TIMEOUT 2       /* an mbarrier wait ran out of time                */
 #define OSCAR_DEVERR_SEQ_LEN 4       /* a length or position outside its valid range    */
+#define OSCAR_DEVERR_NONFINITE 8     /* a group of rotated values held a NaN or an
+                                        infinity; it was stored as a zero group
+                                        (s = z = 0, codes 0)                            */
 
 #define OSCAR_VARIANT_OSCAR 0        /* R = U H P_br                                    */
 #define OSCAR_VARIANT_HADAMARD 1     /* R = H (data-oblivious baseline)                 */
@@ -167,6 +174,29 @@ oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k,
 oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_new,
                                    const void* v_new, const int32_t* seq_lens_after,
                                    int32_t batch, void* stream);
+
+/* Diagnostic forms of the two placement calls: the same kernels, the same pool
+ * bytes, and in addition the fp32 rotated values y = x R that each INT2
+ * placement computed before clipping, so that a test can check the rotation
+ * (against x R in higher precision) apart from the decisions that follow it
+ * (clip, group range, s, z, codes: a function of y alone).  The pages describe
+ * no such output.
+ *   oscar_prefill_quantize_trace: y_out device fp32
+ *     [total_tokens][num_kv_heads][2][d] (index 0 keys, 1 values); rows of
+ *     tokens placed in BF16 slots are not written.
+ *   oscar_quantize_append_trace: y_out device fp32 [batch][num_kv_heads][2][d],
+ *     the values of the token that leaves the window (rows of sequences with
+ *     no leaving token are not written).
+ * y_out 16-byte aligned or null (null: the plain call).  Other arguments as
+ * oscar_prefill_quantize / oscar_quantize_append. */
+oscar_status oscar_prefill_quantize_trace(const oscar_cache_desc* desc, const void* k,
+                                          const void* v, const int32_t* seq_ids,
+                                          const int32_t* positions, const int32_t* seq_lens_final,
+                                          int32_t num_seqs, int64_t total_tokens, float* y_out,
+                                          void* stream);
+oscar_status oscar_quantize_append_trace(const oscar_cache_desc* desc, const void* k_new,
+                                         const void* v_new, const int32_t* seq_lens_after,
+                                         int32_t batch, float* y_out, void* stream);
 
 /* Bytes of device workspace oscar_decode_attention / _bf16 need for this batch
  * and maximum sequence length (depends on the device's SM count). */

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "liboscar.so")
 OSCAR_OK = 0
 STATUS_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "WORKSPACE", -4: "CUDA",
                 -5: "NOT_CONVERGED"}
-DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SEQ_LEN = 1, 2, 4
+DEVERR_PAGE_ID, DEVERR_TIMEOUT, DEVERR_SEQ_LEN, DEVERR_NONFINITE = 1, 2, 4, 8
 VARIANT_OSCAR, VARIANT_HADAMARD, VARIANT_IDENTITY = 0, 1, 2
 EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rotation",
             "oscar_prefill_quantize", "oscar_quantize_append", "oscar_decode_workspace_size",
@@ -29,7 +29,8 @@ EXPORTED = ("oscar_query_covariance", "oscar_score_covariance", "oscar_build_rot
             "oscar_multiquery_workspace_size", "oscar_decode_step_host_staging_size",
             "oscar_decode_step_host",
             "oscar_calibration_workspace_size", "oscar_query_covariance_device",
-            "oscar_score_covariance_device", "oscar_clip_threshold_device")
+            "oscar_score_covariance_device", "oscar_clip_threshold_device",
+            "oscar_prefill_quantize_trace", "oscar_quantize_append_trace")
 
 
 class OscarError(RuntimeError):
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
             "oscar_build_rotation": (I32, [I32, P, P, I64, D, I32, P, P, P, P]),
             "oscar_prefill_quantize": (I32, [P, P, P, P, P, P, I32, I64, P]),
             "oscar_quantize_append": (I32, [P, P, P, P, I32, P]),
+            "oscar_prefill_quantize_trace": (I32, [P, P, P, P, P, P, I32, I64, P, P]),
+            "oscar_quantize_append_trace": (I32, [P, P, P, P, I32, P, P]),
             "oscar_decode_workspace_size": (ctypes.c_size_t, [P, I32, I32]),
             "oscar_multiquery_workspace_size": (ctypes.c_size_t, [P, I32, I32, I32]),
             "oscar_decode_attention": (I32, [P, P, P, I32, I32, P, P, ctypes.c_size_t, P]),
@@ -220,6 +223,28 @@ def oscar_quantize_append(cache: Cache, k_new, v_new, seq_lens_after, stream=Non
            lib().oscar_quantize_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new),
                                        _ptr(seq_lens_after), int(seq_lens_after.numel()),
                                        _stream(stream)))
+
+
+def oscar_prefill_quantize_trace(cache: Cache, k, v, seq_ids, positions, seq_lens_final, y_out,
+                                 stream=None):
+    """oscar_prefill_quantize that also writes the fp32 rotated values of every
+    INT2 placement to y_out (float32 [total_tokens, Hkv, 2, d], device)."""
+    d = cache.desc()
+    _check("oscar_prefill_quantize_trace",
+           lib().oscar_prefill_quantize_trace(ctypes.byref(d), _ptr(k), _ptr(v), _ptr(seq_ids),
+                                              _ptr(positions), _ptr(seq_lens_final),
+                                              int(seq_lens_final.numel()), int(seq_ids.numel()),
+                                              _ptr(y_out), _stream(stream)))
+
+
+def oscar_quantize_append_trace(cache: Cache, k_new, v_new, seq_lens_after, y_out, stream=None):
+    """oscar_quantize_append that also writes the fp32 rotated values of each
+    token leaving the window to y_out (float32 [batch, Hkv, 2, d], device)."""
+    d = cache.desc()
+    _check("oscar_quantize_append_trace",
+           lib().oscar_quantize_append_trace(ctypes.byref(d), _ptr(k_new), _ptr(v_new),
+                                             _ptr(seq_lens_after), int(seq_lens_after.numel()),
+                                             _ptr(y_out), _stream(stream)))
 
 
 def oscar_decode_workspace_size(cache: Cache, batch: int, max_seq_len: int) -> int:

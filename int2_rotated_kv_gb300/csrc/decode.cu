@@ -58,6 +58,7 @@ struct DecodeParams {
   const int32_t* bf16_pt;
   const float* r_k;
   const float* r_v;
+  const float* clip_v;
   int32_t* status;
   const uint16_t* q;
   uint16_t* out;
@@ -138,8 +139,13 @@ struct SplitCfg {
   static constexpr int kScratch = kDWarps * (16 + 8 * D) * 4;
   static_assert(kScratch <= kRing, "merge scratch reuses the ring");
   static constexpr int kIds = 0;                                      // int [kMaxCtaPages]
-  static constexpr int kLps = kIds + kMaxCtaPages * 4;               // int [kMaxCtaPages]
-  static constexpr int kBars = kLps + kMaxCtaPages * 4;              // u64 [warps][stages]
+  // the BF16 split's logical pages; in an INT2 split the same bytes hold the
+  // query operands: q' as fp16 hi and lo fragments ([D/16][32] uint2 each),
+  // then the zero-term operand (uint32 [32])
+  static constexpr int kLps = kIds + kMaxCtaPages * 4;
+  static constexpr int kQOperands = 2 * (D / 16) * 32 * 8 + 32 * 4;
+  static constexpr int kLpsBytes = kMaxCtaPages * 4 > kQOperands ? kMaxCtaPages * 4 : kQOperands;
+  static constexpr int kBars = (kLps + kLpsBytes + 15) / 16 * 16;    // u64 [warps][stages]
   static constexpr int kRingOff = kBars + kDWarps * 8 * 8;
   static constexpr int kBytes = kRingOff + kRing;
   static constexpr int kCtasPerSm = kBf16Only ? 1 : 2;
@@ -191,10 +197,11 @@ __device__ __forceinline__ void softmax_tile(Softmax& st, float (&l)[4], float (
 
 // Same update for two 16-token tiles at once (one vote, one rescale).  The
 // probability sum is accumulated elsewhere (ones row of the zero-term MMA).
+// The probabilities come out weighed by 2^pe (see int2_pscale_log2).
 template <int NT>
 __device__ __forceinline__ void softmax_pair(Softmax& st, float (&la)[4], float (&lb)[4],
                                              float (&o)[NT][4], float (&z)[4], float (&pa)[4],
-                                             float (&pb)[4]) {
+                                             float (&pb)[4], float pe) {
   float mx0 = fmaxf(fmaxf(la[0], la[2]), fmaxf(lb[0], lb[2]));
   float mx1 = fmaxf(fmaxf(la[1], la[3]), fmaxf(lb[1], lb[3]));
   if (__any_sync(0xffffffffu, mx0 > st.m0 + kTau || mx1 > st.m1 + kTau)) {
@@ -214,12 +221,26 @@ __device__ __forceinline__ void softmax_pair(Softmax& st, float (&la)[4], float 
     z[0] *= a0; z[1] *= a1; z[2] *= a0; z[3] *= a1;
     st.m0 = n0; st.m1 = n1;
   }
-  const float b0 = st.m0 == -INFINITY ? 0.f : st.m0;
-  const float b1 = st.m1 == -INFINITY ? 0.f : st.m1;
+  const float b0 = (st.m0 == -INFINITY ? 0.f : st.m0) - pe;
+  const float b1 = (st.m1 == -INFINITY ? 0.f : st.m1) - pe;
   pa[0] = fast_exp2(la[0] - b0); pa[1] = fast_exp2(la[1] - b1);
   pa[2] = fast_exp2(la[2] - b0); pa[3] = fast_exp2(la[3] - b1);
   pb[0] = fast_exp2(lb[0] - b0); pb[1] = fast_exp2(lb[1] - b1);
   pb[2] = fast_exp2(lb[2] - b0); pb[3] = fast_exp2(lb[3] - b1);
+}
+
+// Exponent pe of the power-of-two weight 2^pe the INT2 probabilities carry
+// into p.V.  There the tensor cores see p and p * s in fp16, with p <= 2^kTau
+// (the lazily raised running max) and s <= fp16((max - min)/3) <= 2 clip / 3
+// (the group range lies inside [-clip, clip]).  pe is the largest exponent
+// with 2^pe * 2^kTau * s_max <= 2^15 (at most 7, so 2^pe p stays below fp16's
+// largest value): p * s never overflows and small p * s stay out of fp16's
+// subnormal range as far as the headroom allows.  The weight cancels out of
+// the split's results (output and probability sum are divided by it).
+__device__ __forceinline__ float int2_pscale_log2(float clip_v) {
+  const float smax = fminf(65504.f, fmaxf(clip_v, 0.f) * (2.f / 3.f) * 1.001f);
+  if (!(smax > 0.f)) return 7.f;
+  return fmaxf(-24.f, fminf(7.f, floorf(log2f(32768.f / (exp2f(kTau) * smax)))));
 }
 
 // The query columns of one split CTA.  MMA column c (0..7) holds query head
@@ -277,9 +298,13 @@ __device__ __forceinline__ void load_words(const uint8_t* base, int lane, uint32
 // read as INT2 codes; the high plane's dot products weigh 4.  Each group's dot
 // products are weighed by the token's key scale, and the sum is brought to
 // log2-domain logits by one multiply-add onto the zero term.
+// The query enters as an fp16 pair, q' = hi + lo (lo the fp16 rounding of what
+// hi leaves): both products with a code are exact and the pair carries q' to
+// ~2^-22, so a logit's error does not grow with |q'| beyond fp32 accumulation.
 template <int D, int P, int NPG>
 __device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const uint2* qbs,
-                                        uint32_t qz, float ks, int lane, float (&lg)[NPG][4]) {
+                                        const uint2* qbl, uint32_t qz, float ks, int lane,
+                                        float (&lg)[NPG][4]) {
   using F = Fmt<D, P>;
   constexpr int NG = D / 32;
   const int gid = lane >> 2, tig = lane & 3;
@@ -315,19 +340,30 @@ __device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const u
     // by 8, so every extracted half is code * 4^i * 16^(s&1) * 2^-24
     const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
     const uint2 b0 = qbs[(2 * m) * 32 + lane], b1 = qbs[(2 * m + 1) * 32 + lane];
+    const uint2 c0 = qbl[(2 * m) * 32 + lane], c1 = qbl[(2 * m + 1) * 32 + lane];
 #pragma unroll
     for (int pg = 0; pg < NPG; ++pg) {
       float dg[4];
       {   // A registers a0..a3 hold key pairs s = 0, 2, 1, 3 (lowest plane)
         const uint32_t wl = kw[pg][P - 1][m], wh = kw[pg][P - 1][m] >> 8;
-        mma_f16_z(dg, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
-        mma_f16(dg, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+        const uint32_t a0 = wl & m0, a1 = wh & m0, a2 = wl & m1, a3 = wh & m1;
+        const uint32_t e0 = wl & (m0 << 2), e1 = wh & (m0 << 2), e2 = wl & (m1 << 2),
+                       e3 = wh & (m1 << 2);
+        mma_f16_z(dg, a0, a1, a2, a3, b0.x, b0.y);
+        mma_f16(dg, e0, e1, e2, e3, b1.x, b1.y);
+        mma_f16(dg, a0, a1, a2, a3, c0.x, c0.y);
+        mma_f16(dg, e0, e1, e2, e3, c1.x, c1.y);
       }
       if constexpr (P == 2) {   // high plane: code bits 3..2
         const uint32_t wl = kw[pg][0][m], wh = kw[pg][0][m] >> 8;
+        const uint32_t a0 = wl & m0, a1 = wh & m0, a2 = wl & m1, a3 = wh & m1;
+        const uint32_t e0 = wl & (m0 << 2), e1 = wh & (m0 << 2), e2 = wl & (m1 << 2),
+                       e3 = wh & (m1 << 2);
         float dh[4];
-        mma_f16_z(dh, wl & m0, wh & m0, wl & m1, wh & m1, b0.x, b0.y);
-        mma_f16(dh, wl & (m0 << 2), wh & (m0 << 2), wl & (m1 << 2), wh & (m1 << 2), b1.x, b1.y);
+        mma_f16_z(dh, a0, a1, a2, a3, b0.x, b0.y);
+        mma_f16(dh, e0, e1, e2, e3, b1.x, b1.y);
+        mma_f16(dh, a0, a1, a2, a3, c0.x, c0.y);
+        mma_f16(dh, e0, e1, e2, e3, c1.x, c1.y);
 #pragma unroll
         for (int k = 0; k < 4; ++k) dg[k] = fmaf(4.f, dh[k], dg[k]);
       }
@@ -446,7 +482,8 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
   // ---- query operand, once the rotated query is complete: warp 0 reads q'
   // once and stages the MMA operand and the zero-term operand for every warp
   pdl_wait();
-  uint32_t* qzs = reinterpret_cast<uint32_t*>(qbs + NK * 32);
+  uint2* qbl = qbs + NK * 32;                                 // the lo halves of the pair
+  uint32_t* qzs = reinterpret_cast<uint32_t*>(qbs + 2 * NK * 32);
   if (warp == 0) {
     uint32_t qz = 0;
     // this lane's column gid: head qh0 + gid % G of row row0 + gid / G when
@@ -467,9 +504,14 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
       }
       gs[kk >> 1] += (v0.x + v0.y) + (v1.x + v1.y);
       // codes of k-step parity i and channel half h are read at 4^i * 16^h
+      // (exact power-of-two weights); each weighted value becomes an fp16 pair
       const float sc = (kk & 1) ? 0.25f : 1.f;
-      qbs[kk * 32 + lane] = make_uint2(pack_half2(v0.x * sc, v0.y * sc),
-                                       pack_half2(v1.x * sc * 0.0625f, v1.y * sc * 0.0625f));
+      const float w0 = v0.x * sc, w1 = v0.y * sc;
+      const float w2 = v1.x * sc * 0.0625f, w3 = v1.y * sc * 0.0625f;
+      const uint32_t h01 = pack_half2(w0, w1), h23 = pack_half2(w2, w3);
+      qbs[kk * 32 + lane] = make_uint2(h01, h23);
+      qbl[kk * 32 + lane] = make_uint2(pack_half2(w0 - half_lo(h01), w1 - half_hi(h01)),
+                                       pack_half2(w2 - half_lo(h23), w3 - half_hi(h23)));
     }
     float mine = 0.f;
 #pragma unroll
@@ -501,6 +543,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     }
   }
   const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
+  const float pe = int2_pscale_log2(p.clip_v[h]);
   // every column sees INT2 tokens in [tok_lo, tok_hi); column 2tig (2tig+1)
   // sees them below min(L - window, lim0 (lim1)), worked out where a page needs masking
   const int tok_lo = p.sink, tok_hi = min(L - p.window, cs.lim_lo);
@@ -516,7 +559,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     float lab[2][4];
     {
       const uint8_t* const sts[2] = {stA, stB};
-      int2_qk<D, P, 2>(sts, qbs, qz, ks, lane, lab);
+      int2_qk<D, P, 2>(sts, qbs, qbl, qz, ks, lane, lab);
     }
     float (&la)[4] = lab[0];
     float (&lb)[4] = lab[1];
@@ -543,7 +586,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
       }
     }
     float pa[4], pbv[4];
-    softmax_pair<NK>(sm, la, lb, o, zacc, pa, pbv);
+    softmax_pair<NK>(sm, la, lb, o, zacc, pa, pbv, pe);
     int2_pv<D, P>(stA, pa, lane, o, zacc);
     int2_pv<D, P>(stB, pbv, lane, o, zacc);
     __syncwarp();
@@ -567,7 +610,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     float l1[1][4];
     {
       const uint8_t* const sts[1] = {stA};
-      int2_qk<D, P, 1>(sts, qbs, qz, ks, lane, l1);
+      int2_qk<D, P, 1>(sts, qbs, qbl, qz, ks, lane, l1);
     }
     float (&la)[4] = l1[0];
     const int pA = (lo + warp + kDWarps * i) * kPage;
@@ -585,7 +628,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     }
     float pa[4];
     float dummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, pd[4];
-    softmax_pair<NK>(sm, la, dummy, o, zacc, pa, pd);
+    softmax_pair<NK>(sm, la, dummy, o, zacc, pa, pd, pe);
     int2_pv<D, P>(stA, pa, lane, o, zacc);
   }
 }
@@ -846,10 +889,12 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
 
   // ---- warp result -> shared scratch (the ring is idle once every warp is here)
   float l0 = sm.l0, l1 = sm.l1;
+  // INT2 pages: every probability carried the weight 2^pe
+  const float unw = mode == 0 ? exp2f(-int2_pscale_log2(p.clip_v[h])) : 1.f;
   if (mode == 0) {
     // INT2 pages: the probability sum sits on row NG of the zero-term accumulator
-    l0 = __shfl_sync(0xffffffffu, zacc[0], NG * 4 + tig);
-    l1 = __shfl_sync(0xffffffffu, zacc[1], NG * 4 + tig);
+    l0 = __shfl_sync(0xffffffffu, zacc[0], NG * 4 + tig) * unw;
+    l1 = __shfl_sync(0xffffffffu, zacc[1], NG * 4 + tig) * unw;
   } else {
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -877,9 +922,10 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
     const int c0 = 16 * mt + gid, c1 = c0 + 8;
     float v0 = o[mt][0], v1 = o[mt][1], v2 = o[mt][2], v3 = o[mt][3];
     if (mode == 0) {
-      // undo the code read-out scale: 2^24 / 4^(mt&1), and / 16 for rows gid+8
-      const float sc = (mt & 1) ? 4194304.f : 16777216.f;
-      const float za = zz0[mt >> 1], zb = zz1[mt >> 1];
+      // undo the code read-out scale: 2^24 / 4^(mt&1), and / 16 for rows gid+8,
+      // and the probabilities' weight
+      const float sc = ((mt & 1) ? 4194304.f : 16777216.f) * unw;
+      const float za = zz0[mt >> 1] * unw, zb = zz1[mt >> 1] * unw;
       v0 = fmaf(v0, sc, za); v1 = fmaf(v1, sc, zb);
       v2 = fmaf(v2, sc * 0.0625f, za); v3 = fmaf(v3, sc * 0.0625f, zb);
     }
@@ -1203,6 +1249,7 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.bf16_pt = c->bf16_page_table;
   p.r_k = c->r_k;
   p.r_v = c->r_v;
+  p.clip_v = c->clip_v;
   p.status = c->status;
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);

@@ -59,6 +59,10 @@ struct QuantParams {
   // the rotated query is also written, rounded to bf16, to qrope [B][Hq][D]
   double rope_log2_base;
   uint16_t* qrope;
+  // optional diagnostic output: the fp32 rotated values y = x R each INT2
+  // placement computed (before clipping), [item][Hkv][2 (K, V)][D]; entries of
+  // items without an INT2 placement are not written
+  float* y_out;
 };
 
 template <int D>
@@ -269,7 +273,13 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams p
     for (int task = warp; task < kQTile * NG; task += kQThreads / 32) {
       const int t = task / NG, grp = task % NG;
       if (m_i2page[t] < 0) continue;
-      const float y = ys[t * D + 32 * grp + lane];
+      float y = ys[t * D + 32 * grp + lane];
+      if (p.y_out)
+        p.y_out[((tile * kQTile + t) * p.hkv + h) * (2 * D) + kv * D + 32 * grp + lane] = y;
+      if (__any_sync(0xffffffffu, !isfinite(y))) {   // stored as a zero group
+        if (lane == 0) flag(p.status, OSCAR_DEVERR_NONFINITE);
+        y = 0.f;
+      }
       const float yc = fminf(fmaxf(y, -clip), clip);
       const float mn = warp_min(yc);
       const float mx = warp_max(yc);
@@ -529,7 +539,12 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
       acc[2] = fmaf(xv.z, rs[i + 2][lane], acc[2]);
       acc[3] = fmaf(xv.w, rs[i + 3][lane], acc[3]);
     }
-    const float y = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    float y = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    if (p.y_out) p.y_out[(static_cast<int64_t>(b) * p.hkv + h) * (2 * D) + kv * D + j] = y;
+    if (__any_sync(0xffffffffu, !isfinite(y))) {   // stored as a zero group
+      if (lane == 0) flag(p.status, OSCAR_DEVERR_NONFINITE);
+      y = 0.f;
+    }
     const float yc = fminf(fmaxf(y, -clip), clip);
     const float mn = warp_min(yc);
     const float mx = warp_max(yc);
@@ -654,15 +669,17 @@ oscar_status append_with_query(const oscar_cache_desc* desc, const void* q, cons
 
 extern "C" {
 
-oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k, const void* v,
-                                    const int32_t* seq_ids, const int32_t* positions,
-                                    const int32_t* seq_lens_final, int32_t num_seqs,
-                                    int64_t total_tokens, void* stream) {
+oscar_status oscar_prefill_quantize_trace(const oscar_cache_desc* desc, const void* k,
+                                          const void* v, const int32_t* seq_ids,
+                                          const int32_t* positions, const int32_t* seq_lens_final,
+                                          int32_t num_seqs, int64_t total_tokens, float* y_out,
+                                          void* stream) {
   oscar_status s = oscar_host::check_desc(desc, true, true);
   if (s != OSCAR_OK) return s;
   if (total_tokens < 0 || num_seqs < 1) return OSCAR_ERR_INVALID_ARG;
   if (total_tokens == 0) return OSCAR_OK;
   if (!k || !v || !seq_ids || !positions || !seq_lens_final) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(y_out) & 15) return OSCAR_ERR_INVALID_ARG;
   oscar::QuantParams p = oscar::base_params(desc);
   p.append = 0;
   p.n_items = total_tokens;
@@ -672,6 +689,7 @@ oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k,
   p.seq_ids = seq_ids;
   p.positions = positions;
   p.seq_lens = seq_lens_final;
+  p.y_out = y_out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the rotation on the tensor cores whenever the inputs suit TMA; the
   // CUDA-core kernel otherwise (same bytes either way)
@@ -682,14 +700,23 @@ oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k,
   return oscar::dispatch(p, desc->head_dim, st);
 }
 
-oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_new,
-                                   const void* v_new, const int32_t* seq_lens_after,
-                                   int32_t batch, void* stream) {
+oscar_status oscar_prefill_quantize(const oscar_cache_desc* desc, const void* k, const void* v,
+                                    const int32_t* seq_ids, const int32_t* positions,
+                                    const int32_t* seq_lens_final, int32_t num_seqs,
+                                    int64_t total_tokens, void* stream) {
+  return oscar_prefill_quantize_trace(desc, k, v, seq_ids, positions, seq_lens_final, num_seqs,
+                                      total_tokens, nullptr, stream);
+}
+
+oscar_status oscar_quantize_append_trace(const oscar_cache_desc* desc, const void* k_new,
+                                         const void* v_new, const int32_t* seq_lens_after,
+                                         int32_t batch, float* y_out, void* stream) {
   oscar_status s = oscar_host::check_desc(desc, true, true);
   if (s != OSCAR_OK) return s;
   if (batch < 0) return OSCAR_ERR_INVALID_ARG;
   if (batch == 0) return OSCAR_OK;
   if (!k_new || !v_new || !seq_lens_after) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(y_out) & 15) return OSCAR_ERR_INVALID_ARG;
   oscar::QuantParams p = oscar::base_params(desc);
   p.append = 1;
   p.n_items = batch;
@@ -697,8 +724,15 @@ oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_n
   p.k_src = static_cast<const uint16_t*>(k_new);
   p.v_src = static_cast<const uint16_t*>(v_new);
   p.seq_lens = seq_lens_after;
+  p.y_out = y_out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return desc->head_dim == 128 ? oscar::launch_append<128>(p, st) : oscar::launch_append<64>(p, st);
+}
+
+oscar_status oscar_quantize_append(const oscar_cache_desc* desc, const void* k_new,
+                                   const void* v_new, const int32_t* seq_lens_after,
+                                   int32_t batch, void* stream) {
+  return oscar_quantize_append_trace(desc, k_new, v_new, seq_lens_after, batch, nullptr, stream);
 }
 
 }  // extern "C"

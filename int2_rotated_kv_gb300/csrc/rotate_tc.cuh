@@ -417,6 +417,13 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       __syncwarp();
       if (lane == 0) tc_arrive(&acc_empty[buf]);
       if (i2 < 0) continue;
+      if (p.y_out) {   // diagnostic: the rotated values this row's decisions start from
+        float4* yo = reinterpret_cast<float4*>(
+            p.y_out + ((tile * kTcM + row) * p.hkv + h) * (2 * D) + kv * D + 32 * grp);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4)
+          yo[j4] = make_float4(y[4 * j4], y[4 * j4 + 1], y[4 * j4 + 2], y[4 * j4 + 3]);
+      }
       const int slot = i2 % kPage;
       using F = Fmt<D, P>;
       constexpr int kMaxCode = P == 2 ? 15 : 3;   // INT4 variant / INT2
@@ -425,11 +432,18 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       // the clipped extremes of the raw values, and a value beyond the clip
       // threshold lands on code 0 or the top code either way: the values
       // themselves are never clipped on this path.
+      // A NaN carries through min.NaN / max.NaN and an infinity ends up as an
+      // extreme, so the group is finite exactly when both extremes are; a
+      // non-finite group is stored as a zero group (s = z = 0: every code 0).
       float mn = y[0], mx = y[0];
 #pragma unroll
       for (int j = 1; j < 32; ++j) {
-        mn = fminf(mn, y[j]);
-        mx = fmaxf(mx, y[j]);
+        mn = fmin_nan(mn, y[j]);
+        mx = fmax_nan(mx, y[j]);
+      }
+      if (!(isfinite(mn) && isfinite(mx))) {
+        flag(p.status, OSCAR_DEVERR_NONFINITE);
+        mn = mx = 0.f;
       }
       mn = fminf(fmaxf(mn, -clip), clip);
       mx = fminf(fmaxf(mx, -clip), clip);

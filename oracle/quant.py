@@ -19,6 +19,14 @@ precision of the library's kernels, step by step:
     code = 0 if s16 == 0 else clamp(rint( fp32( fp32(yc - z16) / s16 ) ), 0, 3)
 Dequantisation is y_hat = code * s16 + z16.
 
+Non-finite values (a reading: the pages are silent).  Under IEEE arithmetic a
+NaN or an infinity anywhere in x makes every entry of y = x R non-finite (an
+infinity times a zero entry of R is NaN, otherwise it stays infinite or meets
+another one of opposite sign), so ``rotate`` returns a row of NaN for such an
+x.  A group whose fp32 values y32 are not all finite is stored as a zero group:
+s16 = z16 = 0 and every code 0 (its dequantised values are 0, and the library
+reports it in its status word).
+
 INT4 variant (a format variant beside the pages' INT2, for the comparison the
 pages draw with INT4 caches in [Summary 4]): the same steps with 16 levels, i.e.
 the divisor 3 and the top code 3 become 15 (``levels`` = largest code).
@@ -33,22 +41,30 @@ INT4_MAX_CODE = 15    # 16 levels
 
 
 def rotate(x: np.ndarray, r: np.ndarray) -> np.ndarray:
-    """y = x R in fp64 (x holds bf16 values, R fp32 values; each product is exact)."""
-    return np.asarray(x, np.float64) @ np.asarray(r, np.float64)
+    """y = x R in fp64 (x holds bf16 values, R fp32 values; each product is
+    exact).  A row of x with a non-finite entry gives a row of NaN (see above)."""
+    x = np.asarray(x, np.float64)
+    bad = ~np.isfinite(x).all(axis=-1)
+    y = np.where(bad[..., None], 0.0, x) @ np.asarray(r, np.float64)
+    return np.where(bad[..., None], np.nan, y)
 
 
 def quantize(y: np.ndarray, clip: float, group: int = GROUP, levels: int = INT2_MAX_CODE):
     """Quantise rotated vectors y [..., d] to codes 0..levels.  Returns (codes
     uint8 [..., d], s16 float16 [..., d/group], z16 float16 [..., d/group])."""
-    y32 = np.asarray(y).astype(np.float32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        y32 = np.asarray(y).astype(np.float32)
     c = np.float32(clip)
-    yc = np.minimum(np.maximum(y32, -c), c)
-    shp = yc.shape
+    shp = y32.shape
     d = shp[-1]
     ng = d // group
+    # groups with a non-finite value are stored as zero groups
+    bad = ~np.isfinite(y32.reshape(shp[:-1] + (ng, group))).all(axis=-1)
+    y32 = np.where(np.repeat(bad, group, axis=-1).reshape(shp), np.float32(0), y32)
+    yc = np.minimum(np.maximum(y32, -c), c)
     g = yc.reshape(shp[:-1] + (ng, group))
-    mn = g.min(axis=-1)
-    mx = g.max(axis=-1)
+    mn = np.where(bad, np.float32(0), g.min(axis=-1))
+    mx = np.where(bad, np.float32(0), g.max(axis=-1))
     s32 = np.float32(mx - mn) / np.float32(levels)
     s16 = s32.astype(np.float32).astype(np.float16)
     z16 = mn.astype(np.float16)
@@ -58,6 +74,14 @@ def quantize(y: np.ndarray, clip: float, group: int = GROUP, levels: int = INT2_
         code = np.clip(np.rint(t), 0, levels)
     code = np.where((s16 == 0)[..., None], 0, code)
     return code.reshape(shp).astype(np.uint8), s16, z16
+
+
+def nonfinite_groups(y: np.ndarray, group: int = GROUP) -> np.ndarray:
+    """bool [..., d/group]: groups ``quantize`` stores as zero groups."""
+    with np.errstate(over="ignore", invalid="ignore"):
+        y32 = np.asarray(y).astype(np.float32)
+    shp = y32.shape
+    return ~np.isfinite(y32.reshape(shp[:-1] + (shp[-1] // group, group))).all(axis=-1)
 
 
 def dequantize(codes: np.ndarray, s16: np.ndarray, z16: np.ndarray, group: int = GROUP) -> np.ndarray:

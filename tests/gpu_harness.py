@@ -216,3 +216,124 @@ def check_close(got, ref, what=""):
 def kappa(d):
     # sequential fp32 FMA chain of d terms: |error| <= d * 2^-24 * sum |x_i R_ij|
     return 1.01 * d * 2.0 ** -24
+
+
+# ---------------------------------------------------------------- traced placement
+#
+# The quantising kernels' diagnostic forms return the fp32 rotated values y they
+# computed.  That splits the check of a placement in two:
+#   rotation:  |y_kernel - x R| <= kappa * sum_i |x_i| |R_ij|, with x R exact (fp64)
+#              and kappa the a-priori error bound of the kernel's fp32 arithmetic;
+#   decisions: clip, group range, s16, z16 and every code are a function of y
+#              alone, so the stored entries must equal the oracle's quantiser
+#              applied to y_kernel, bit for bit, in every group (no exemptions).
+
+# tensor-core prefill: x (bf16) times R split into three bf16 pieces, products
+# exact, 3d of them summed in fp32 by the tensor core (truncating adds allowed)
+def kappa_tc(d):
+    return 3 * d * 2.0 ** -23
+
+
+def prefill_trace(cache, inst, lens=None, upto=None, misalign=False):
+    """As ``prefill`` through oscar_prefill_quantize_trace.  Returns
+    (y float32 [T, Hkv, 2, d], {b: (first item, count)})."""
+    t = torch()
+    lens = inst.seq_lens if lens is None else np.asarray(lens)
+    H = inst.workload.num_kv_heads
+    ks, vs, sid, pos, where = [], [], [], [], {}
+    at = 0
+    for b, L in enumerate(lens):
+        n = int(L) if upto is None else int(upto[b])
+        ks.append(np.stack([inst.k[b][h][:n] for h in range(H)], 1))
+        vs.append(np.stack([inst.v[b][h][:n] for h in range(H)], 1))
+        sid.append(np.full(n, b, np.int32))
+        pos.append(np.arange(n, dtype=np.int32))
+        where[b] = (at, n)
+        at += n
+    k = bf16_tensor(np.concatenate(ks))
+    v = bf16_tensor(np.concatenate(vs))
+    if misalign:
+        k, v = misaligned_copy(k), misaligned_copy(v)
+    y = t.full((at, H, 2, inst.workload.head_dim), float("nan"), dtype=t.float32, device=DEV)
+    L = lib()
+    L.oscar_prefill_quantize_trace(cache, k, v, t.from_numpy(np.concatenate(sid)).to(DEV),
+                                   t.from_numpy(np.concatenate(pos)).to(DEV),
+                                   t.from_numpy(np.asarray(lens, np.int32)).to(DEV), y)
+    t.cuda.synchronize()
+    return y.cpu().numpy(), where
+
+
+def stored_int2(cache, pp, b, h, positions, d, bits=2, pools_=None):
+    """The INT2 entries the pools hold for positions of sequence b, KV head h:
+    (kc, ks, kz, vc, vs, vz), codes [n, d], scales and zeros [n, d/32]."""
+    got2 = pools(cache)[0] if pools_ is None else pools_
+    hkv = cache.num_kv_heads
+    blk = layout.int2_block_bytes(d, bits)
+    positions = np.asarray(positions, np.int64)
+    n, ng = positions.size, d // 32
+    out = [np.zeros((n, d), np.uint8), np.zeros((n, ng), np.float16), np.zeros((n, ng), np.float16),
+           np.zeros((n, d), np.uint8), np.zeros((n, ng), np.float16), np.zeros((n, ng), np.float16)]
+    for pg in np.unique(positions // 16):
+        sel = np.flatnonzero(positions // 16 == pg)
+        pid = int(pp.int2_table[b, pg])
+        parts = layout.unpack_int2_block(got2[(pid * hkv + h) * blk:(pid * hkv + h + 1) * blk], d, bits)
+        slots = positions[sel] - 16 * pg
+        for o, part in zip(out, parts):
+            o[sel] = part[slots]
+    return tuple(out)
+
+
+def check_traced(cache, pp, inst, rot, rows, kappa, *, lens, sink, window, bits=2, pools_=None):
+    """Rotation and decision checks of traced placements.
+
+    rows: {b: (positions, y float32 [n, Hkv, 2, d])}; only positions in the
+    INT2 region of sequence b (length lens[b]) are checked.  Returns counts:
+    groups checked, the largest |y_kernel - x R| / sum |x| |R| seen, and the
+    groups whose stored entries differ from the oracle's placement from the
+    exact x R (allowed only where y_kernel and x R straddle a decision)."""
+    levels = quant.INT2_MAX_CODE if bits == 2 else quant.INT4_MAX_CODE
+    w = inst.workload
+    d, hkv = w.head_dim, w.num_kv_heads
+    got2 = pools(cache)[0] if pools_ is None else pools_
+    groups = straddle = 0
+    worst = 0.0
+    for b, (positions, yb) in rows.items():
+        positions = np.asarray(positions, np.int64)
+        m = ocache.is_int2(positions, int(lens[b]), sink, window)
+        ti, yb = positions[m], yb[m]
+        if ti.size == 0:
+            continue
+        for h in range(hkv):
+            st = stored_int2(cache, pp, b, h, ti, d, bits, got2)
+            for kv, (xs, r, c, (sc, ss, sz)) in enumerate((
+                    (inst.k, rot.rk[h], rot.ck[h], st[:3]), (inst.v, rot.rv[h], rot.cv[h], st[3:]))):
+                x = np.asarray(xs[b][h], np.float64)[ti]
+                yk = yb[:, h, kv, :].astype(np.float64)
+                assert np.isfinite(yk).all(), "a traced INT2 placement wrote no rotated values"
+                ye = quant.rotate(x, r)
+                bnd = np.abs(x) @ np.abs(np.asarray(r, np.float64))
+                err = np.abs(yk - ye)
+                assert (err <= kappa * bnd).all(), \
+                    f"rotation error {float((err / np.maximum(bnd, 1e-300)).max()):.3e} beyond {kappa:.3e}"
+                worst = max(worst, float((err / np.maximum(bnd, 1e-300)).max()))
+                qc, qs, qz = quant.quantize(yk, c, levels=levels)
+                np.testing.assert_array_equal(sc, qc, err_msg=f"codes, seq {b} head {h} kv {kv}")
+                np.testing.assert_array_equal(ss.view(np.uint16), qs.view(np.uint16))
+                np.testing.assert_array_equal(sz.view(np.uint16), qz.view(np.uint16))
+                ec, es, ez = quant.quantize(ye, c, levels=levels)
+                differs = ((ec != qc).reshape(len(ti), -1, 32).any(-1) | (es.view(np.uint16) != qs.view(np.uint16))
+                           | (ez.view(np.uint16) != qz.view(np.uint16)))
+                groups += differs.size
+                straddle += int(differs.sum())
+    return {"groups": groups, "max_rotation_error_ratio": worst, "straddling_groups": straddle}
+
+
+def report(name, **stats):
+    """Append one JSON line of parity statistics to the file named by the
+    environment variable OSCAR_PARITY_REPORT (nothing when it is unset)."""
+    import json
+    import os
+    path = os.environ.get("OSCAR_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"test": name, **stats}) + "\n")

@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import golden_io
-from oracle import quant
+from oracle import quant, rotation
 
 
 def test_hand_worked_groups():
@@ -152,3 +152,48 @@ def test_int4_flags_cover_only_near_boundary_entries():
     # finer levels put more entries near a decision boundary than INT2 does
     e2, _ = quant.near_boundary_flags(x, r, 2.0, kappa=2.0 ** -16)
     assert elem.mean() >= e2.mean() and elem.mean() < 0.05
+
+
+def test_nonfinite_groups_are_zero_groups():
+    """Reading for non-finite values: a group whose fp32 rotated values are not
+    all finite is stored as s = z = 0 with every code 0; the other groups of the
+    same vector are quantised as if it were absent."""
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal((3, 128))
+    y[0, 40] = np.nan            # group 1 of row 0
+    y[1, 127] = np.inf           # group 3 of row 1
+    y[2, 0] = 1e39               # finite in fp64, infinite in fp32: group 0 of row 2
+    codes, s16, z16 = quant.quantize(y, 2.5)
+    bad = np.zeros((3, 4), bool)
+    bad[0, 1] = bad[1, 3] = bad[2, 0] = True
+    np.testing.assert_array_equal(quant.nonfinite_groups(y), bad)
+    for r, g in zip(*np.nonzero(bad)):
+        assert s16[r, g] == 0 and z16[r, g] == 0
+        assert not codes[r, 32 * g:32 * g + 32].any()
+    for r in range(3):
+        for g in range(4):
+            if bad[r, g]:
+                continue
+            c1, s1, z1 = quant.quantize(y[r, 32 * g:32 * g + 32][None], 2.5)
+            np.testing.assert_array_equal(codes[r, 32 * g:32 * g + 32], c1[0])
+            assert s16[r, g] == s1[0, 0] and z16[r, g] == z1[0, 0]
+
+
+def test_nonfinite_input_poisons_the_whole_rotated_row():
+    """IEEE arithmetic: one NaN or infinity in x makes every entry of x R
+    non-finite, whatever R (an infinity times a zero entry is NaN), so every
+    group of that token-head becomes a zero group; other rows are untouched."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((3, 64))
+    x[0, 3] = np.inf
+    x[1, 60] = np.nan
+    for r in (np.eye(64), rotation.hadamard(64)):
+        y = quant.rotate(x, r)
+        assert np.isnan(y[:2]).all()
+        np.testing.assert_allclose(y[2], x[2] @ r, rtol=1e-15, atol=1e-15)
+        # direct IEEE evaluation agrees on which entries are finite
+        with np.errstate(invalid="ignore"):
+            direct = np.array([[np.sum(x[i] * r[:, j]) for j in range(64)] for i in range(2)])
+        assert not np.isfinite(direct).any()
+        codes, s16, z16 = quant.quantize(y, 1.0)
+        assert not codes[:2].any() and not s16[:2].any() and not z16[:2].any()
