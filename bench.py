@@ -463,6 +463,38 @@ def time_e2e(dec, steps, warmup):
     return e0.elapsed_time(e1) / steps, hin.numel() * 2, ho.numel() * 2
 
 
+def fidelity_leg(inst, di, rot_oscar, dev, n_calib):
+    """Attention-output error of the INT2 cache against the same-design BF16
+    kernel on the same context, for OSCAR, Hadamard-only and unrotated INT2
+    (the comparison the pages draw): rotations from the library's calibration
+    calls, one fused decode step each, rel-L2 of the outputs.  A report, not a
+    target."""
+    torch = __import__("torch")
+    from int2_rotated_kv_gb300 import _lib as L
+    rots = {"oscar": rot_oscar}
+    for name, var in (("hadamard_only", L.VARIANT_HADAMARD), ("unrotated", L.VARIANT_IDENTITY)):
+        rk, rv, ck, cv = [], [], [], []
+        for h in range(inst.workload.num_kv_heads):
+            _, r_k, c_k, _ = L.oscar_build_rotation(None, inst.calib_k[h][:n_calib], 99.9, var)
+            _, r_v, c_v, _ = L.oscar_build_rotation(None, inst.calib_v[h][:n_calib], 99.9, var)
+            rk.append(r_k); rv.append(r_v); ck.append(c_k); cv.append(c_v)
+        rots[name] = (np.stack(rk), np.stack(rv), np.array(ck, np.float32), np.array(cv, np.float32))
+
+    def out_of(dec):
+        dec.step(0)
+        torch.cuda.synchronize()
+        return dec.out.float().cpu().numpy().astype(np.float64)
+    ref = out_of(Decoder(di, rot_oscar, dev, bf16_only=True))
+    res = {"workload": inst.workload.name, "context": int(inst.seq_lens.max()),
+           "metric": "rel-L2 of the decode output against the same-design BF16 kernel's",
+           "n_calib": n_calib}
+    for name, rot in rots.items():
+        o = out_of(Decoder(di, rot, dev))
+        res[name] = round(float(np.linalg.norm(o - ref) / max(np.linalg.norm(ref), 1e-300)), 5)
+    torch.cuda.empty_cache()
+    return res
+
+
 # -------------------------------------------------------------- CPU / oracle
 
 def oracle_sample(inst, rot, n_heads=1, max_tokens=None):
@@ -993,6 +1025,11 @@ def main():
         "setup_s": {"generate": round(t_gen, 1), "calibrate": round(t_cal, 1)},
     }
     out.update(bf)
+    if rank == 0:
+        try:
+            out["fidelity"] = fidelity_leg(inst, di, rot, dev, n_calib)
+        except Exception as e:
+            out["fidelity"] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
     if args.extras and rank == 0:
         ex = {}
         del dec

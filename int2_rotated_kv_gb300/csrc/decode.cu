@@ -34,6 +34,7 @@
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -58,6 +59,7 @@ struct DecodeParams {
   const int32_t* bf16_pt;
   const float* r_k;
   const float* r_v;
+  const float* clip_k;
   const float* clip_v;
   int32_t* status;
   const uint16_t* q;
@@ -143,7 +145,7 @@ struct SplitCfg {
   // query operands: q' as fp16 hi and lo fragments ([D/16][32] uint2 each),
   // then the zero-term operand (uint32 [32])
   static constexpr int kLps = kIds + kMaxCtaPages * 4;
-  static constexpr int kQOperands = 2 * (D / 16) * 32 * 8 + 32 * 4;
+  static constexpr int kQOperands = 2 * (D / 16) * 32 * 8 + 32 * 4 + 16;
   static constexpr int kLpsBytes = kMaxCtaPages * 4 > kQOperands ? kMaxCtaPages * 4 : kQOperands;
   static constexpr int kBars = (kLps + kLpsBytes + 15) / 16 * 16;    // u64 [warps][stages]
   static constexpr int kRingOff = kBars + kDWarps * 8 * 8;
@@ -243,6 +245,22 @@ __device__ __forceinline__ float int2_pscale_log2(float clip_v) {
   return fmaxf(-24.f, fminf(7.f, floorf(log2f(32768.f / (exp2f(kTau) * smax)))));
 }
 
+// The INT2 loop's precision, chosen once per split CTA.  With q' and p * s in
+// fp16 alone (2^-12 relative) the error of an output element grows with the
+// size of the logits and of the values; the fast loop is kept where both stay
+// at the scale of unit-variance activations with outliers (|logits| below
+// 2^4 in log2 units, bounded by max |q'| * clip_K / sqrt(d) / ln 2, and a value
+// clip below 32, where the measured error of the fast loop is below a quarter
+// of the output tolerance), and the precise loop (fp16 pairs for both,
+// ~2^-22) runs otherwise.
+constexpr float kFastLogitLog2 = 16.f;
+constexpr float kFastValueClip = 32.f;
+
+__device__ __forceinline__ bool split_precise(float qmax, float clip_k, float clip_v,
+                                              float scale_log2) {
+  return !(qmax * fabsf(clip_k) * scale_log2 <= kFastLogitLog2 && fabsf(clip_v) <= kFastValueClip);
+}
+
 // The query columns of one split CTA.  MMA column c (0..7) holds query head
 // qh0 + c % gq of batch row row0 + c / gq, for c < gq * nrows (the rest are
 // unused).  lim0 / lim1: the visibility limits (positions below) of this
@@ -298,10 +316,11 @@ __device__ __forceinline__ void load_words(const uint8_t* base, int lane, uint32
 // read as INT2 codes; the high plane's dot products weigh 4.  Each group's dot
 // products are weighed by the token's key scale, and the sum is brought to
 // log2-domain logits by one multiply-add onto the zero term.
-// The query enters as an fp16 pair, q' = hi + lo (lo the fp16 rounding of what
-// hi leaves): both products with a code are exact and the pair carries q' to
-// ~2^-22, so a logit's error does not grow with |q'| beyond fp32 accumulation.
-template <int D, int P, int NPG>
+// kPrecise: the query enters as an fp16 pair, q' = hi + lo (lo the fp16
+// rounding of what hi leaves): both products with a code are exact and the pair
+// carries q' to ~2^-22.  Otherwise q' enters as fp16 alone (2^-12 relative),
+// which the split CTA allows only for logits of moderate size (split_precise).
+template <int D, int P, int NPG, bool kPrecise>
 __device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const uint2* qbs,
                                         const uint2* qbl, uint32_t qz, float ks, int lane,
                                         float (&lg)[NPG][4]) {
@@ -340,7 +359,11 @@ __device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const u
     // by 8, so every extracted half is code * 4^i * 16^(s&1) * 2^-24
     const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
     const uint2 b0 = qbs[(2 * m) * 32 + lane], b1 = qbs[(2 * m + 1) * 32 + lane];
-    const uint2 c0 = qbl[(2 * m) * 32 + lane], c1 = qbl[(2 * m + 1) * 32 + lane];
+    uint2 c0 = make_uint2(0u, 0u), c1 = make_uint2(0u, 0u);
+    if constexpr (kPrecise) {
+      c0 = qbl[(2 * m) * 32 + lane];
+      c1 = qbl[(2 * m + 1) * 32 + lane];
+    }
 #pragma unroll
     for (int pg = 0; pg < NPG; ++pg) {
       float dg[4];
@@ -351,8 +374,10 @@ __device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const u
                        e3 = wh & (m1 << 2);
         mma_f16_z(dg, a0, a1, a2, a3, b0.x, b0.y);
         mma_f16(dg, e0, e1, e2, e3, b1.x, b1.y);
-        mma_f16(dg, a0, a1, a2, a3, c0.x, c0.y);
-        mma_f16(dg, e0, e1, e2, e3, c1.x, c1.y);
+        if constexpr (kPrecise) {
+          mma_f16(dg, a0, a1, a2, a3, c0.x, c0.y);
+          mma_f16(dg, e0, e1, e2, e3, c1.x, c1.y);
+        }
       }
       if constexpr (P == 2) {   // high plane: code bits 3..2
         const uint32_t wl = kw[pg][0][m], wh = kw[pg][0][m] >> 8;
@@ -362,8 +387,10 @@ __device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const u
         float dh[4];
         mma_f16_z(dh, a0, a1, a2, a3, b0.x, b0.y);
         mma_f16(dh, e0, e1, e2, e3, b1.x, b1.y);
-        mma_f16(dh, a0, a1, a2, a3, c0.x, c0.y);
-        mma_f16(dh, e0, e1, e2, e3, c1.x, c1.y);
+        if constexpr (kPrecise) {
+          mma_f16(dh, a0, a1, a2, a3, c0.x, c0.y);
+          mma_f16(dh, e0, e1, e2, e3, c1.x, c1.y);
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) dg[k] = fmaf(4.f, dh[k], dg[k]);
       }
@@ -387,14 +414,23 @@ __device__ __forceinline__ void int2_qk(const uint8_t* const (&st)[NPG], const u
 
 // p.V for one INT2 page-head: o (channel x query head) += codes^T (p * s), plus
 // the zero term and, on the spare row NG, the probability sum (ones row).
-template <int D, int P>
+// kPrecise: p enters as an fp16 pair p = hi + lo, and p * s as the pair
+// (fp16(hi s), the rounding of (hi s - fp16(hi s)) + lo s), the first residual
+// exact by a fused multiply-add: both to ~2^-22 instead of fp16's 2^-12.
+template <int D, int P, bool kPrecise>
 __device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4], int lane,
                                         float (&o)[D / 16][4], float (&zacc)[4]) {
   using F = Fmt<D, P>;
   constexpr int NG = D / 32;
   const int gid = lane >> 2, tig = lane & 3;
-  const uint32_t pb0 = movmatrix_trans(pack_half2(pr[0], pr[1]));
-  const uint32_t pb1 = movmatrix_trans(pack_half2(pr[2], pr[3]));
+  const uint32_t h01 = pack_half2(pr[0], pr[1]), h23 = pack_half2(pr[2], pr[3]);
+  const uint32_t pb0 = movmatrix_trans(h01);
+  const uint32_t pb1 = movmatrix_trans(h23);
+  uint32_t pl0 = 0u, pl1 = 0u;
+  if constexpr (kPrecise) {
+    pl0 = movmatrix_trans(pack_half2(pr[0] - half_lo(h01), pr[1] - half_hi(h01)));
+    pl1 = movmatrix_trans(pack_half2(pr[2] - half_lo(h23), pr[3] - half_hi(h23)));
+  }
   uint32_t vw[P][NG], vs0[NG], vs1[NG];
 #pragma unroll
   for (int pl = 0; pl < P; ++pl) load_words<NG>(st + F::kVc + pl * F::kPlane, lane, vw[pl]);
@@ -414,21 +450,39 @@ __device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4],
   for (int m = 0; m < NG; ++m) {
     const uint32_t bb0 = hmul2_u32(pb0, vs0[m]);
     const uint32_t bb1 = hmul2_u32(pb1, vs1[m]);
+    uint32_t bl0 = 0u, bl1 = 0u;
+    if constexpr (kPrecise) {
+      bl0 = hfma2_u32(pl0, vs0[m], hfma2_u32(pb0, vs0[m], bb0 ^ 0x80008000u));
+      bl1 = hfma2_u32(pl1, vs1[m], hfma2_u32(pb1, vs1[m], bb1 ^ 0x80008000u));
+    }
     // value pair s = r: rows gid (s = 0, 2) read at 4^i, rows gid+8 (s = 1, 3) at 16 * 4^i
     const uint32_t m0 = 0x00030003u, m1 = 0x00300030u;
     {   // lowest plane
       const uint32_t wl = vw[P - 1][m], wh = vw[P - 1][m] >> 8;
-      mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bb0, bb1);
-      mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
-              bb0, bb1);
+      const uint32_t a0 = wl & m0, a1 = wl & m1, a2 = wh & m0, a3 = wh & m1;
+      const uint32_t e0 = wl & (m0 << 2), e1 = wl & (m1 << 2), e2 = wh & (m0 << 2),
+                     e3 = wh & (m1 << 2);
+      mma_f16(o[2 * m], a0, a1, a2, a3, bb0, bb1);
+      mma_f16(o[2 * m + 1], e0, e1, e2, e3, bb0, bb1);
+      if constexpr (kPrecise) {
+        mma_f16(o[2 * m], a0, a1, a2, a3, bl0, bl1);
+        mma_f16(o[2 * m + 1], e0, e1, e2, e3, bl0, bl1);
+      }
     }
     if constexpr (P == 2) {   // high plane, weighed by 4 (exact in fp16)
       const uint32_t four = 0x44004400u;
       const uint32_t bh0 = hmul2_u32(bb0, four), bh1 = hmul2_u32(bb1, four);
       const uint32_t wl = vw[0][m], wh = vw[0][m] >> 8;
-      mma_f16(o[2 * m], wl & m0, wl & m1, wh & m0, wh & m1, bh0, bh1);
-      mma_f16(o[2 * m + 1], wl & (m0 << 2), wl & (m1 << 2), wh & (m0 << 2), wh & (m1 << 2),
-              bh0, bh1);
+      const uint32_t a0 = wl & m0, a1 = wl & m1, a2 = wh & m0, a3 = wh & m1;
+      const uint32_t e0 = wl & (m0 << 2), e1 = wl & (m1 << 2), e2 = wh & (m0 << 2),
+                     e3 = wh & (m1 << 2);
+      mma_f16(o[2 * m], a0, a1, a2, a3, bh0, bh1);
+      mma_f16(o[2 * m + 1], e0, e1, e2, e3, bh0, bh1);
+      if constexpr (kPrecise) {
+        const uint32_t bm0 = hmul2_u32(bl0, four), bm1 = hmul2_u32(bl1, four);
+        mma_f16(o[2 * m], a0, a1, a2, a3, bm0, bm1);
+        mma_f16(o[2 * m + 1], e0, e1, e2, e3, bm0, bm1);
+      }
     }
   }
   const uint32_t* vz = reinterpret_cast<const uint32_t*>(st + F::kVz);
@@ -440,6 +494,7 @@ __device__ __forceinline__ void int2_pv(const uint8_t* st, const float (&pr)[4],
     za0 = za2 = 0x3C003C00u;   // ones: row NG accumulates sum_t p
   }
   mma_f16(zacc, za0, 0u, za2, 0u, pb0, pb1);
+  if constexpr (kPrecise) mma_f16(zacc, za0, 0u, za2, 0u, pl0, pl1);
 }
 
 // INT2 pages [lo, lo + n) of one (sequence, KV head): warp w takes pages
@@ -493,6 +548,7 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     const int chead = kPacked ? gid % G : gid;
     const float* qr = p.qrot + (static_cast<size_t>(cs.row0 + crow) * p.hq + cs.qh0 + chead) * D;
     float gs[NG];
+    float qmax = 0.f;
 #pragma unroll
     for (int g = 0; g < NG; ++g) gs[g] = 0.f;
 #pragma unroll
@@ -502,6 +558,8 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
         v0 = __ldcg(reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig));
         v1 = __ldcg(reinterpret_cast<const float2*>(qr + 16 * kk + 2 * tig + 8));
       }
+      qmax = fmax_nan(qmax, fmax_nan(fmax_nan(fabsf(v0.x), fabsf(v0.y)),
+                                     fmax_nan(fabsf(v1.x), fabsf(v1.y))));
       gs[kk >> 1] += (v0.x + v0.y) + (v1.x + v1.y);
       // codes of k-step parity i and channel half h are read at 4^i * 16^h
       // (exact power-of-two weights); each weighted value becomes an fp16 pair
@@ -528,9 +586,16 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
            (static_cast<uint32_t>(__half_as_ushort(lo16)) << 16);
     }
     qzs[lane] = qz;
+    // a NaN query takes the precise loop (either propagates it)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      qmax = fmax_nan(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+    if (lane == 0)
+      qzs[32] = split_precise(qmax, p.clip_k[h], p.clip_v[h], p.scale_log2) ? 1u : 0u;
   }
   __syncthreads();
   const uint32_t qz = qzs[lane];
+  const bool precise = qzs[32] != 0u;
   if (lane == 0) {
     if (deferred >= 0) {
       mbar_arrive_expect_tx(&wbar[deferred], SB);
@@ -542,95 +607,104 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
       bulk_g2s(wring + i * SB, pool_h + max(wids[kDWarps * i], 0) * pstride, SB, &wbar[i]);
     }
   }
-  const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
-  const float pe = int2_pscale_log2(p.clip_v[h]);
-  // every column sees INT2 tokens in [tok_lo, tok_hi); column 2tig (2tig+1)
-  // sees them below min(L - window, lim0 (lim1)), worked out where a page needs masking
-  const int tok_lo = p.sink, tok_hi = min(L - p.window, cs.lim_lo);
-  uint32_t phase = 0;
-  int s = 0;
-  int i = 0;
-  for (; i + 1 < my_n; i += 2) {
-    const int idA = wids[kDWarps * i], idB = wids[kDWarps * (i + 1)];
-    if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
-    if (!wait_stage<NS, true>(wbar, s + 1, phase, i + 1, my_n, ids, warp, p.status)) return;
-    const uint8_t* stA = wring + s * SB;
-    const uint8_t* stB = stA + SB;
-    float lab[2][4];
-    {
-      const uint8_t* const sts[2] = {stA, stB};
-      int2_qk<D, P, 2>(sts, qbs, qbl, qz, ks, lane, lab);
+  // the page loop in the precision the CTA chose (two instantiations)
+  auto loop = [&](auto precise_tag) {
+    constexpr bool kPrecise = decltype(precise_tag)::value;
+    const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
+    const float pe = int2_pscale_log2(p.clip_v[h]);
+    // every column sees INT2 tokens in [tok_lo, tok_hi); column 2tig (2tig+1)
+    // sees them below min(L - window, lim0 (lim1)), worked out where a page needs masking
+    const int tok_lo = p.sink, tok_hi = min(L - p.window, cs.lim_lo);
+    uint32_t phase = 0;
+    int s = 0;
+    int i = 0;
+    for (; i + 1 < my_n; i += 2) {
+      const int idA = wids[kDWarps * i], idB = wids[kDWarps * (i + 1)];
+      if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
+      if (!wait_stage<NS, true>(wbar, s + 1, phase, i + 1, my_n, ids, warp, p.status)) return;
+      const uint8_t* stA = wring + s * SB;
+      const uint8_t* stB = stA + SB;
+      float lab[2][4];
+      {
+        const uint8_t* const sts[2] = {stA, stB};
+        int2_qk<D, P, 2, kPrecise>(sts, qbs, qbl, qz, ks, lane, lab);
+      }
+      float (&la)[4] = lab[0];
+      float (&lb)[4] = lab[1];
+      const int pA = (lo + warp + kDWarps * i) * kPage, pB = pA + kDWarps * kPage;
+      if (pA < tok_lo || pB + kPage > tok_hi || (idA | idB) < 0) {
+        const int t0 = pA + gid, t1 = t0 + 8, u0 = pB + gid, u1 = u0 + 8;
+        if constexpr (kPacked) {   // each column its own row's limit
+          const int hi0 = min(L - p.window, cs.lim0), hi1 = min(L - p.window, cs.lim1);
+          const bool a0 = idA >= 0 && t0 >= tok_lo, a1 = idA >= 0 && t1 >= tok_lo;
+          const bool c0 = idB >= 0 && u0 >= tok_lo, c1 = idB >= 0 && u1 >= tok_lo;
+          if (!(a0 && t0 < hi0)) la[0] = -INFINITY;
+          if (!(a0 && t0 < hi1)) la[1] = -INFINITY;
+          if (!(a1 && t1 < hi0)) la[2] = -INFINITY;
+          if (!(a1 && t1 < hi1)) la[3] = -INFINITY;
+          if (!(c0 && u0 < hi0)) lb[0] = -INFINITY;
+          if (!(c0 && u0 < hi1)) lb[1] = -INFINITY;
+          if (!(c1 && u1 < hi0)) lb[2] = -INFINITY;
+          if (!(c1 && u1 < hi1)) lb[3] = -INFINITY;
+        } else {
+          if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
+          if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
+          if (idB < 0 || u0 < tok_lo || u0 >= tok_hi) lb[0] = lb[1] = -INFINITY;
+          if (idB < 0 || u1 < tok_lo || u1 >= tok_hi) lb[2] = lb[3] = -INFINITY;
+        }
+      }
+      float pa[4], pbv[4];
+      softmax_pair<NK>(sm, la, lb, o, zacc, pa, pbv, pe);
+      int2_pv<D, P, kPrecise>(stA, pa, lane, o, zacc);
+      int2_pv<D, P, kPrecise>(stB, pbv, lane, o, zacc);
+      __syncwarp();
+      if (lane == 0) {
+        if (i + NS < my_n) {
+          mbar_arrive_expect_tx(&wbar[s], SB);
+          bulk_g2s(wring + s * SB, pool_h + max(wids[kDWarps * (i + NS)], 0) * pstride, SB, &wbar[s]);
+        }
+        if (i + 1 + NS < my_n) {
+          mbar_arrive_expect_tx(&wbar[s + 1], SB);
+          bulk_g2s(wring + (s + 1) * SB, pool_h + max(wids[kDWarps * (i + 1 + NS)], 0) * pstride,
+                   SB, &wbar[s + 1]);
+        }
+      }
+      s = (s + 2 == NS) ? 0 : s + 2;
     }
-    float (&la)[4] = lab[0];
-    float (&lb)[4] = lab[1];
-    const int pA = (lo + warp + kDWarps * i) * kPage, pB = pA + kDWarps * kPage;
-    if (pA < tok_lo || pB + kPage > tok_hi || (idA | idB) < 0) {
-      const int t0 = pA + gid, t1 = t0 + 8, u0 = pB + gid, u1 = u0 + 8;
-      if constexpr (kPacked) {   // each column its own row's limit
+    if (i < my_n) {   // odd tail: one page
+      const int idA = wids[kDWarps * i];
+      if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
+      const uint8_t* stA = wring + s * SB;
+      float l1[1][4];
+      {
+        const uint8_t* const sts[1] = {stA};
+        int2_qk<D, P, 1, kPrecise>(sts, qbs, qbl, qz, ks, lane, l1);
+      }
+      float (&la)[4] = l1[0];
+      const int pA = (lo + warp + kDWarps * i) * kPage;
+      const int t0 = pA + gid, t1 = t0 + 8;
+      if constexpr (kPacked) {
         const int hi0 = min(L - p.window, cs.lim0), hi1 = min(L - p.window, cs.lim1);
         const bool a0 = idA >= 0 && t0 >= tok_lo, a1 = idA >= 0 && t1 >= tok_lo;
-        const bool c0 = idB >= 0 && u0 >= tok_lo, c1 = idB >= 0 && u1 >= tok_lo;
         if (!(a0 && t0 < hi0)) la[0] = -INFINITY;
         if (!(a0 && t0 < hi1)) la[1] = -INFINITY;
         if (!(a1 && t1 < hi0)) la[2] = -INFINITY;
         if (!(a1 && t1 < hi1)) la[3] = -INFINITY;
-        if (!(c0 && u0 < hi0)) lb[0] = -INFINITY;
-        if (!(c0 && u0 < hi1)) lb[1] = -INFINITY;
-        if (!(c1 && u1 < hi0)) lb[2] = -INFINITY;
-        if (!(c1 && u1 < hi1)) lb[3] = -INFINITY;
       } else {
         if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
         if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
-        if (idB < 0 || u0 < tok_lo || u0 >= tok_hi) lb[0] = lb[1] = -INFINITY;
-        if (idB < 0 || u1 < tok_lo || u1 >= tok_hi) lb[2] = lb[3] = -INFINITY;
       }
+      float pa[4];
+      float dummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, pd[4];
+      softmax_pair<NK>(sm, la, dummy, o, zacc, pa, pd, pe);
+      int2_pv<D, P, kPrecise>(stA, pa, lane, o, zacc);
     }
-    float pa[4], pbv[4];
-    softmax_pair<NK>(sm, la, lb, o, zacc, pa, pbv, pe);
-    int2_pv<D, P>(stA, pa, lane, o, zacc);
-    int2_pv<D, P>(stB, pbv, lane, o, zacc);
-    __syncwarp();
-    if (lane == 0) {
-      if (i + NS < my_n) {
-        mbar_arrive_expect_tx(&wbar[s], SB);
-        bulk_g2s(wring + s * SB, pool_h + max(wids[kDWarps * (i + NS)], 0) * pstride, SB, &wbar[s]);
-      }
-      if (i + 1 + NS < my_n) {
-        mbar_arrive_expect_tx(&wbar[s + 1], SB);
-        bulk_g2s(wring + (s + 1) * SB, pool_h + max(wids[kDWarps * (i + 1 + NS)], 0) * pstride,
-                 SB, &wbar[s + 1]);
-      }
-    }
-    s = (s + 2 == NS) ? 0 : s + 2;
-  }
-  if (i < my_n) {   // odd tail: one page
-    const int idA = wids[kDWarps * i];
-    if (!wait_stage<NS, true>(wbar, s, phase, i, my_n, ids, warp, p.status)) return;
-    const uint8_t* stA = wring + s * SB;
-    float l1[1][4];
-    {
-      const uint8_t* const sts[1] = {stA};
-      int2_qk<D, P, 1>(sts, qbs, qbl, qz, ks, lane, l1);
-    }
-    float (&la)[4] = l1[0];
-    const int pA = (lo + warp + kDWarps * i) * kPage;
-    const int t0 = pA + gid, t1 = t0 + 8;
-    if constexpr (kPacked) {
-      const int hi0 = min(L - p.window, cs.lim0), hi1 = min(L - p.window, cs.lim1);
-      const bool a0 = idA >= 0 && t0 >= tok_lo, a1 = idA >= 0 && t1 >= tok_lo;
-      if (!(a0 && t0 < hi0)) la[0] = -INFINITY;
-      if (!(a0 && t0 < hi1)) la[1] = -INFINITY;
-      if (!(a1 && t1 < hi0)) la[2] = -INFINITY;
-      if (!(a1 && t1 < hi1)) la[3] = -INFINITY;
-    } else {
-      if (idA < 0 || t0 < tok_lo || t0 >= tok_hi) la[0] = la[1] = -INFINITY;
-      if (idA < 0 || t1 < tok_lo || t1 >= tok_hi) la[2] = la[3] = -INFINITY;
-    }
-    float pa[4];
-    float dummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, pd[4];
-    softmax_pair<NK>(sm, la, dummy, o, zacc, pa, pd, pe);
-    int2_pv<D, P>(stA, pa, lane, o, zacc);
-  }
+
+  };
+  if (precise)
+    loop(std::true_type{});
+  else
+    loop(std::false_type{});
 }
 
 // BF16 pages (the sink + recent split, or every page of the BF16 baseline):
@@ -1249,6 +1323,7 @@ oscar_status decode_entry(const oscar_cache_desc* c, const void* q, const int32_
   p.bf16_pt = c->bf16_page_table;
   p.r_k = c->r_k;
   p.r_v = c->r_v;
+  p.clip_k = c->clip_k;
   p.clip_v = c->clip_v;
   p.status = c->status;
   p.q = static_cast<const uint16_t*>(q);

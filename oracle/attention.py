@@ -147,17 +147,43 @@ def calibrate(calib_q, calib_k, calib_v, variant: int, percentile: float = 99.9)
     return cache.Rotations(rk, rv, ck, cv)
 
 
-def fidelity_report(inst, *, sink: int, window: int) -> dict:
-    """rel-L2 of the mixed-cache output against all-BF16 attention for the three
-    rotations the pages compare ([Summary 1], [Summary 4]).  A report only:
-    the pages print no number this could be pinned to (parity unpinned)."""
+FIDELITY_VARIANTS = (("oscar", rotation.OSCAR), ("hadamard_only", rotation.HADAMARD_ONLY),
+                     ("unrotated", rotation.IDENTITY))
+
+
+def fidelity_report(inst, *, sink: int, window: int, rotations: dict | None = None) -> dict:
+    """How far the mixed cache moves attention from the all-BF16 cache, for the
+    three rotations the pages compare: OSCAR, Hadamard only and none
+    ([Summary 1], [Summary 4], [Abstract]).  Per variant:
+      out_rel_l2  rel-L2 of the decode output against all-BF16 attention;
+      k_rel_l2, v_rel_l2  rel-L2 of the INT2 tokens' reconstructed keys and
+      values (original basis) against the stored bf16 ones.
+    ``rotations`` optionally maps a variant name to its Rotations (default:
+    ``calibrate`` on the instance's calibration sets).  The pages print no
+    number for this synthetic setting, so only its special cases are pinned
+    (no INT2 token gives zero error; values already on the four-level grid
+    are reproduced exactly without rotation)."""
     w = inst.workload
     ref = bf16_decode(inst.q, inst.k, inst.v, inst.seq_lens, gqa=w.gqa)
     out = {}
-    for name, var in (("oscar", rotation.OSCAR), ("hadamard_only", rotation.HADAMARD_ONLY),
-                      ("unrotated", rotation.IDENTITY)):
-        rot = calibrate(inst.calib_q, inst.calib_k, inst.calib_v, var)
+    for name, var in FIDELITY_VARIANTS:
+        rot = (rotations or {}).get(name) or calibrate(inst.calib_q, inst.calib_k, inst.calib_v, var)
         o = mixed_decode(inst.q, inst.k, inst.v, inst.seq_lens, rot, sink=sink, window=window,
                          gqa=w.gqa)
-        out[name] = rel_l2(o, ref)
+        dk = nk = dv = nv = 0.0
+        for b, L in enumerate(inst.seq_lens):
+            L = int(L)
+            m = cache.is_int2(np.arange(L), L, sink, window)
+            for h in range(w.num_kv_heads):
+                ke, ve = effective_kv(inst.k[b][h], inst.v[b][h], L, sink, window,
+                                      rot.rk[h], rot.rv[h], rot.ck[h], rot.cv[h])
+                k0 = np.asarray(inst.k[b][h][:L], np.float64)[m]
+                v0 = np.asarray(inst.v[b][h][:L], np.float64)[m]
+                dk += float(((ke[m] - k0) ** 2).sum())
+                nk += float((k0 ** 2).sum())
+                dv += float(((ve[m] - v0) ** 2).sum())
+                nv += float((v0 ** 2).sum())
+        out[name] = {"out_rel_l2": rel_l2(o, ref),
+                     "k_rel_l2": float(np.sqrt(dk / nk)) if nk > 0 else 0.0,
+                     "v_rel_l2": float(np.sqrt(dv / nv)) if nv > 0 else 0.0}
     return out

@@ -174,3 +174,33 @@ def test_multiquery_ignores_tokens_after_the_row():
     b = attention.mixed_multiquery(q, k2, v2, [300], pos, rot, sink=4, window=64, gqa=4)
     np.testing.assert_array_equal(a[0, 0], b[0, 0])      # row at 250 does not see 260..
     assert np.abs(a[0, 1] - b[0, 1]).max() > 1e-3       # row at 299 does
+
+
+def test_fidelity_report_special_cases():
+    """The fidelity report's pins (the pages print no number for it): with no
+    INT2 token every variant reproduces all-BF16 attention exactly; with keys
+    and values already on a four-level grid (every group spanning 0..3, so
+    s = 1, z = 0 and every code exact) the unrotated cache loses nothing; a
+    quantised cache that does lose information shows a positive error."""
+    w = synth.TINY
+    inst = synth.draw_instance(w, n_calib=128, seq_lens=[60])       # 60 <= 4 + 64: all BF16
+    rep = attention.fidelity_report(inst, sink=4, window=64)
+    for name, _ in attention.FIDELITY_VARIANTS:
+        assert rep[name] == {"out_rel_l2": 0.0, "k_rel_l2": 0.0, "v_rel_l2": 0.0}
+    inst = synth.draw_instance(w, n_calib=128, seq_lens=[300])
+    rng = np.random.default_rng(9)
+    grid = []
+    for _ in range(2):
+        a = rng.integers(0, 4, size=(300, 64)).astype(np.float32)
+        a[:, 0::32] = 0.0
+        a[:, 1::32] = 3.0                     # every group spans exactly [0, 3]
+        grid.append([a])
+    inst_g = __import__("dataclasses").replace(inst, k=[grid[0]], v=[grid[1]])
+    eye = [np.eye(64, dtype=np.float32)]
+    rot_id = cache.Rotations(eye, eye, [np.float32(3.0)], [np.float32(3.0)])
+    rep = attention.fidelity_report(inst_g, sink=4, window=64, rotations={"unrotated": rot_id})
+    assert rep["unrotated"] == {"out_rel_l2": 0.0, "k_rel_l2": 0.0, "v_rel_l2": 0.0}
+    rep = attention.fidelity_report(inst, sink=4, window=64, rotations={"unrotated": rot_id})
+    assert rep["unrotated"]["k_rel_l2"] > 0.1 and rep["unrotated"]["out_rel_l2"] > 0.0
+    for name, _ in attention.FIDELITY_VARIANTS:
+        assert 0.0 < rep[name]["v_rel_l2"] < 1.0
