@@ -52,7 +52,9 @@ def parse():
     ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
     ap.add_argument("--workload", default=synth.QWEN3_8B_32K.name, choices=list(synth.WORKLOADS))
     ap.add_argument("--extras", action="store_true",
-                    help="also time the 128k, prefix-sharing and 40 GB budget workloads (append, prefill)")
+                    help="also time the F1-F4 legs (several query rows, rotary step, calibration, INT4)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other target workloads (128k, batch-64 prefix, 40 GB budget)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-calib", type=int, default=None)
     ap.add_argument("--profile", action="store_true",
@@ -299,7 +301,7 @@ class Decoder:
         self.max_len = int(self.lens.max())
         self.out = torch.zeros((B, hq, d), dtype=torch.bfloat16, device=dev)
         ws = L.oscar_decode_workspace_size(base, B, self.max_len)
-        self.ws = torch.empty(ws // 4 + 64, dtype=torch.float32, device=dev)
+        self.ws = torch.zeros(ws // 4 + 64, dtype=torch.float32, device=dev)
         self.n_layers = n_layers
         self.rope_base = rope_base     # > 0: the fused step with rotary embedding
         self.launches_per_step = 3     # INT2: append+q', split, combine; BF16: append, split, combine
@@ -619,9 +621,16 @@ def decode_leg(di, rot, dev, l2, steps=200, warmup=10, bf16_only=False, code_bit
                   rope_base=rope_base)
     t, clk = time_steps(dec, steps, warmup, clocks=Clocks(gpu_id(torch.cuda.current_device())))
     med, mean = time_decode_calls(dec, 100)
+    peak, peak_kind = peaks()
+    call_gbps = dec.attn_bytes / med / 1e6
+    step_gbps = dec.step_bytes / t / 1e6
     res = {"batch": len(di.seq_lens), "us_per_layer_step": round(t * 1e3, 3),
-           "GBps": round(dec.step_bytes / t / 1e6, 1), "decode_call_us": round(med * 1e3, 3),
-           "decode_call_GBps": round(dec.attn_bytes / med / 1e6, 1),
+           "GBps": round(step_gbps, 1), "decode_call_us": round(med * 1e3, 3),
+           "decode_call_GBps": round(call_gbps, 1),
+           "roofline": {"bound": "hbm", "achieved": round(call_gbps, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(call_gbps / peak, 4), "step_frac": round(step_gbps / peak, 4),
+                        "kernel": "decode call (algorithmic bytes / median CUDA-event time)",
+                        "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None},
            "algorithmic_bytes_per_step": int(dec.step_bytes), "layers_rotated": dec.n_layers,
            "cache_bytes_per_layer": int(dec.layer_bytes), "clocks": clk}
     del dec
@@ -680,7 +689,7 @@ def extra_multiquery(dev, l2, n_calib, rows=16):
     g.manual_seed(3)
     q = torch.randn((1, rows, w.num_q_heads, w.head_dim), generator=g, device=dev).to(torch.bfloat16)
     out = torch.empty_like(q)
-    ws = torch.empty(L.oscar_multiquery_workspace_size(dec.caches[0], 1, rows, Lc) // 4 + 64,
+    ws = torch.zeros(L.oscar_multiquery_workspace_size(dec.caches[0], 1, rows, Lc) // 4 + 64,
                      dtype=torch.float32, device=dev)
     # the caches hold L-1 tokens until a step runs; one step fills the last slot
     for i in range(dec.n_layers):
@@ -857,8 +866,14 @@ def extra_budget(dev, l2, n_calib, budget=40e9):
     dec = Decoder(di, rot, dev, l2_bytes=l2)
     t = time_graph(dec, dec.append, 400, 10)
     nb = append_bytes(dec.lens, w.num_kv_heads, w.head_dim, w.sink, w.window)
+    peak, peak_kind = peaks()
     res["append_b256"] = {"us": round(t * 1e3, 3), "GBps": round(nb / t / 1e6, 1),
-                          "algorithmic_bytes": int(nb)}
+                          "algorithmic_bytes": int(nb),
+                          "roofline": {"bound": "latency", "achieved": round(nb / t / 1e6, 1),
+                                       "peak": peak, "unit": "GB/s",
+                                       "frac": round(nb / t / 1e6 / peak, 4),
+                                       "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None,
+                                       "note": "3.3 MB per call: a chain of dependent loads, not bandwidth"}}
     del dec, di
     torch.cuda.empty_cache()
     # bulk prefill: 256 sequences x 4096 tokens placed in one call
@@ -891,7 +906,11 @@ def extra_budget(dev, l2, n_calib, budget=40e9):
     flops = 2 * 2 * n_i2 * w.num_kv_heads * w.head_dim * w.head_dim
     res["prefill_256x4096"] = {"ms": round(t, 3), "tokens": T, "read_bytes": rd, "write_bytes": wr,
                                "GBps": round((rd + wr) / t / 1e6, 1),
-                               "rotation_TFLOPs": round(flops / t / 1e9, 2)}
+                               "rotation_TFLOPs": round(flops / t / 1e9, 2),
+                               "roofline": {"bound": "hbm", "achieved": round((rd + wr) / t / 1e6, 1),
+                                            "peak": peak, "unit": "GB/s",
+                                            "frac": round((rd + wr) / t / 1e6 / peak, 4),
+                                            "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None}}
     del c, di
     torch.cuda.empty_cache()
     return res
@@ -899,6 +918,9 @@ def extra_budget(dev, l2, n_calib, budget=40e9):
 
 # Extra legs: name -> fn(device, l2_bytes, calibration tokens for the rotations).
 # The calibration leg times calibration itself, on the 8192 tokens of the 8B workload.
+# The other target workloads, measured in every default run beside the headline.
+CONFIG_LEGS = (synth.QWEN3_32B_128K.name, synth.QWEN3_4B_PREFIX.name, synth.QWEN3_8B_BUDGET.name)
+
 EXTRA_LEGS = {
     synth.QWEN3_32B_128K.name: extra_long,
     synth.QWEN3_4B_PREFIX.name: extra_prefix,
@@ -1030,11 +1052,24 @@ def main():
             out["fidelity"] = fidelity_leg(inst, di, rot, dev, n_calib)
         except Exception as e:
             out["fidelity"] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
-    if args.extras and rank == 0:
-        ex = {}
+    if rank == 0 and not args.no_configs:
+        # every other target workload, each with its roofline and clock record
         del dec
         torch.cuda.empty_cache()
+        cf = {}
+        for name in CONFIG_LEGS:
+            try:
+                cf[name] = EXTRA_LEGS[name](dev, l2, 2048)
+            except Exception as e:
+                cf[name] = {"error": f"{type(e).__name__}: {str(e)[:300]}"}
+            torch.cuda.empty_cache()
+        out["configs"] = cf
+    if args.extras and rank == 0:
+        ex = {}
+        torch.cuda.empty_cache()
         for name, fn in EXTRA_LEGS.items():
+            if name in CONFIG_LEGS:
+                continue
             try:
                 ex[name] = fn(dev, l2, 2048)
             except Exception as e:

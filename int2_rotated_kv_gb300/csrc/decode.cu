@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(1024) qrot_kernel(const DecodeParams p) {
 // blocks allow four ring stages per warp at two CTAs per SM)
 template <int D, bool kBf16Only, int P = 1>
 struct SplitCfg {
-  static constexpr int kStagesI = P == 2 ? 4 : 6;        // code-page ring depth per warp
+  // code-page ring depth per warp: 64 bulk copies in flight per SM at two CTAs
+  // per SM (the streaming rate falls with more outstanding copies per SM)
+  static constexpr int kStagesI = 4;
   static constexpr int kStagesB = kBf16Only ? 3 : 1;     // BF16 ring depth per warp
   static constexpr int kRingI = kDWarps * kStagesI * Fmt<D, P>::kInt2Block;
   static constexpr int kRingB = kDWarps * kStagesB * Fmt<D>::kBf16Block;

@@ -84,6 +84,7 @@ __device__ __forceinline__ void flag(int32_t* status, int bit) {
 }  // namespace oscar
 
 #include "rotate_tc.cuh"
+#include "append_group.cuh"
 
 namespace oscar {
 
@@ -380,25 +381,6 @@ oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
 
 // ------------------------------------------------------------------ append
 
-// cos and sin of the rotary angle m * f: the product and its reduction to
-// [-pi, pi] in fp64, then sincosf.
-__device__ __forceinline__ void rope_cs(int m, double f, float& c, float& s) {
-  double a = static_cast<double>(m) * f;
-  a -= 6.283185307179586 * rint(a * 0.15915494309189535);
-  sincosf(static_cast<float>(a), &s, &c);
-}
-
-// Rotary embedding of channel j of a head vector x (pairs j, j +- D/2), fp32,
-// rounded to bf16 (the activation precision).
-template <int D>
-__device__ __forceinline__ float rope_bf16(float xj, float xpartner, int j, int m,
-                                           const double* inv_freq) {
-  float c, s;
-  rope_cs(m, inv_freq[j % (D / 2)], c, s);
-  const float y = j < D / 2 ? __fsub_rn(__fmul_rn(xj, c), __fmul_rn(xpartner, s))
-                            : __fadd_rn(__fmul_rn(xj, c), __fmul_rn(xpartner, s));
-  return __bfloat162float(__float2bfloat16_rn(y));
-}
 //
 // One decode step's append: per sequence b, the new token goes to its BF16 slot
 // (position L-1) and, once L-1-W >= S, the token at L-1-W leaves the window: it
@@ -413,8 +395,6 @@ template <int D, int P>
 __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) {
   constexpr int NG = D / 32;
   using F = Fmt<D, P>;
-  constexpr float kLevels = P == 2 ? 15.f : 3.f;   // largest code: INT4 variant / INT2
-  constexpr int kMaxCode = P == 2 ? 15 : 3;
   __shared__ __align__(16) float rs[D][32];          // R[:, 32*grp .. 32*grp + 31]
   __shared__ __align__(16) float xs[kQThreads / 32][D];
   __shared__ uint8_t cs[kQThreads / 32][32];
@@ -539,59 +519,10 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
       acc[2] = fmaf(xv.z, rs[i + 2][lane], acc[2]);
       acc[3] = fmaf(xv.w, rs[i + 3][lane], acc[3]);
     }
-    float y = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    const float y = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     if (p.y_out) p.y_out[(static_cast<int64_t>(b) * p.hkv + h) * (2 * D) + kv * D + j] = y;
-    if (__any_sync(0xffffffffu, !isfinite(y))) {   // stored as a zero group
-      if (lane == 0) flag(p.status, OSCAR_DEVERR_NONFINITE);
-      y = 0.f;
-    }
-    const float yc = fminf(fmaxf(y, -clip), clip);
-    const float mn = warp_min(yc);
-    const float mx = warp_max(yc);
-    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), kLevels));
-    const __half z16 = __float2half_rn(mn);
-    const float sf = __half2float(s16);
-    const float zf = __half2float(z16);
-    int code = 0;
-    if (sf != 0.f) code = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(yc, zf), sf)), 0), kMaxCode);
-    cs[warp][lane] = static_cast<uint8_t>(code);
-    __syncwarp();
     uint8_t* blk = p.int2_pool + (static_cast<int64_t>(dp) * p.hkv + h) * F::kInt2Block;
-    const uint8_t* ct = cs[warp];
-    if (lane < 8 * P) {   // 8 code bytes of this group per plane; plane 0 = highest bits
-      const int pl = lane >> 3, lb = lane & 7, shift = 2 * (P - 1 - pl);
-      uint32_t byte = 0;
-      if (kv == 0) {
-        const int tig = lb >> 1, e = lb & 1;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            byte |= ((static_cast<uint32_t>(ct[16 * i + 8 * hh + 2 * tig + e]) >> shift) & 3u)
-                    << (4 * hh + 2 * i);
-        blk[F::kKc + pl * F::kPlane + key_byte<D>(slot, tig, grp, e)] = static_cast<uint8_t>(byte);
-      } else {
-        const int gid = lb;
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            byte |= ((static_cast<uint32_t>(ct[16 * i + 8 * ch + gid]) >> shift) & 3u)
-                    << (4 * ch + 2 * i);
-        blk[F::kVc + pl * F::kPlane + value_byte<D>(slot, gid, grp)] = static_cast<uint8_t>(byte);
-      }
-    } else if (lane == 8 * P) {
-      const uint32_t sz = static_cast<uint32_t>(__half_as_ushort(s16)) |
-                          (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
-      if (kv == 0) {
-        reinterpret_cast<uint32_t*>(blk + F::kKsz)[slot * NG + grp] = sz;
-      } else {
-        const int e = vsz_index<D>(slot, grp);
-        reinterpret_cast<uint16_t*>(blk + F::kVs)[e] = static_cast<uint16_t>(sz & 0xffffu);
-        reinterpret_cast<uint16_t*>(blk + F::kVz)[e] = static_cast<uint16_t>(sz >> 16);
-      }
-    }
-    __syncwarp();
+    append_group<D, P>(y, clip, lane, grp, kv, slot, blk, cs[warp], p.status);
   }
 }
 

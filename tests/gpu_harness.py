@@ -126,7 +126,7 @@ def decode(cache, q, lens, max_len=None, bf16_only=False, out=None):
     qt = bf16_tensor(q)
     o = t.zeros((B, Hq, d), dtype=t.bfloat16, device=DEV) if out is None else out
     ws_bytes = L.oscar_decode_workspace_size(cache, B, max_len)
-    ws = t.empty(ws_bytes // 4 + 64, dtype=t.float32, device=DEV)
+    ws = t.zeros(ws_bytes // 4 + 64, dtype=t.float32, device=DEV)
     lt = t.from_numpy(lens).to(DEV)
     fn = L.oscar_decode_attention_bf16 if bf16_only else L.oscar_decode_attention
     fn(cache, qt, lt, max_len, o, ws)

@@ -118,7 +118,7 @@ def test_bad_lengths_are_reported_not_faulted():
     lens = t.tensor([300, 10_000], dtype=t.int32, device=H.DEV)    # beyond max_seq_len
     q = H.bf16_tensor(inst.q)
     o = t.zeros((2, 4, 64), dtype=t.bfloat16, device=H.DEV)
-    ws = t.empty(L.oscar_decode_workspace_size(cache, 2, 300) // 4 + 64, dtype=t.float32,
+    ws = t.zeros(L.oscar_decode_workspace_size(cache, 2, 300) // 4 + 64, dtype=t.float32,
                  device=H.DEV)
     L.oscar_decode_attention(cache, q, lens, 300, o, ws)
     t.cuda.synchronize()

@@ -14,6 +14,9 @@ pytestmark = pytest.mark.gpu
     (synth.TINY, [200, 140, 66], 5, 64),             # d=64, G=4, one KV head; one sequence
                                                       # crosses S+W during the steps
     (synth.QWEN3_8B_32K, [2000, 1503, 133], 3, 128),  # several splits per head
+    # 40 sequences x 8 KV heads: more split CTAs than fit at once, so the step
+    # runs with the append kernel in front instead of as one launch
+    (synth.QWEN3_8B_32K, [300 + 7 * i for i in range(40)], 2, 128),
 ])
 def test_fused_step_equals_append_then_decode(wl, lens0, steps, W):
     t = H.torch()
@@ -29,7 +32,7 @@ def test_fused_step_equals_append_then_decode(wl, lens0, steps, W):
     B, hkv, G = len(lens0), wl.num_kv_heads, wl.gqa
     q = H.bf16_tensor(inst.q)
     max_len = int(lens1.max())
-    ws = t.empty(L.oscar_decode_workspace_size(fused, B, max_len) // 4 + 64, dtype=t.float32,
+    ws = t.zeros(L.oscar_decode_workspace_size(fused, B, max_len) // 4 + 64, dtype=t.float32,
                  device=H.DEV)
     for st in range(steps):
         cur = lens0 + st + 1
@@ -55,6 +58,5 @@ def test_fused_step_equals_append_then_decode(wl, lens0, steps, W):
     np.testing.assert_array_equal(f2, s2)
     np.testing.assert_array_equal(fb, sb)
     exp = H.expected(inst, rot, pp, window=W, lens=lens1, kappa=H.kappa(wl.head_dim))
-    diff, flagged = H.compare_pools(fused, exp)
-    assert diff <= flagged
+    H.compare_pools(fused, exp)   # bytes outside flagged near-boundary entries are exact
     assert H.status(fused) == 0 and H.status(split) == 0

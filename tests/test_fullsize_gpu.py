@@ -47,7 +47,7 @@ def _full_step(wl, heads):
     L.oscar_quantize_append_trace(twin, kn, vn, lt, ya)
     q = H.bf16_tensor(inst.q)
     out = t.zeros(inst.q.shape, dtype=t.bfloat16, device=H.DEV)
-    ws = t.empty(L.oscar_decode_workspace_size(cache, 1, Lc) // 4 + 64, dtype=t.float32, device=H.DEV)
+    ws = t.zeros(L.oscar_decode_workspace_size(cache, 1, Lc) // 4 + 64, dtype=t.float32, device=H.DEV)
     L.oscar_decode_step(cache, q, kn, vn, lt, Lc, out, ws)
     t.cuda.synchronize()
     assert H.status(cache) == 0 and H.status(twin) == 0

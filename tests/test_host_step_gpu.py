@@ -34,7 +34,7 @@ def test_host_step_equals_device_step(wl, lens0, steps, W, rope, pinned):
     H.prefill(dev_c, inst, lens=lens0)
     B, hkv, G = len(lens0), wl.num_kv_heads, wl.gqa
     max_len = int(lens1.max())
-    ws = t.empty(L.oscar_decode_workspace_size(dev_c, B, max_len) // 4 + 64, dtype=t.float32,
+    ws = t.zeros(L.oscar_decode_workspace_size(dev_c, B, max_len) // 4 + 64, dtype=t.float32,
                  device=H.DEV)
     need = L.oscar_decode_step_host_staging_size(host_c, B)
     staging = t.empty(need // 4 + 4, dtype=t.float32, device=H.DEV)
@@ -82,7 +82,7 @@ def test_host_step_rejects_small_staging():
     c, _ = H.make_cache(inst, rot, window=64, lens=lens, growth=1)
     need = L.oscar_decode_step_host_staging_size(c, 1)
     staging = t.empty(need - 16, dtype=t.uint8, device=H.DEV)
-    ws = t.empty(L.oscar_decode_workspace_size(c, 1, 101) // 4 + 64, dtype=t.float32, device=H.DEV)
+    ws = t.zeros(L.oscar_decode_workspace_size(c, 1, 101) // 4 + 64, dtype=t.float32, device=H.DEV)
     in_host = t.zeros(need, dtype=t.uint8).pin_memory()
     out_host = t.zeros(tuple(inst.q.shape), dtype=t.bfloat16).pin_memory()
     lt = t.tensor([101], dtype=t.int32, device=H.DEV)

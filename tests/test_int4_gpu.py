@@ -37,13 +37,24 @@ def test_int4_prefill_exact_rotation_is_bit_exact(wl, lens, misalign):
 @pytest.mark.parametrize("wl,lens,W", [(synth.TINY, [512], 64),
                                        (synth.QWEN3_8B_32K, [1000, 2077, 131], 128)])
 def test_int4_prefill_oscar_rotation_matches_oracle(wl, lens, W, misalign):
+    """As the INT2 test: every group's decisions equal the oracle's sixteen-level
+    quantiser of the kernel's traced rotated values, the rotation lies within
+    its bound, and the pools differ from the exact-x R placement only inside
+    flagged groups where the two values straddle a decision."""
     inst = synth.draw_instance(wl, n_calib=512, seq_lens=lens)
     rot = H.oracle_rotations(inst)
     cache, pp = H.make_cache(inst, rot, window=W, bits=4)
-    H.prefill(cache, inst, misalign=misalign)
-    exp = H.expected(inst, rot, pp, window=W, kappa=H.kappa(wl.head_dim), bits=4)
-    diff, flagged = H.compare_pools(cache, exp)
-    assert diff <= 0.05 * flagged + 8
+    y, where = H.prefill_trace(cache, inst, misalign=misalign)
+    d = wl.head_dim
+    kappa = H.kappa(d) if misalign else H.kappa_tc(d)
+    rows = {b: (np.arange(n), y[s:s + n]) for b, (s, n) in where.items()}
+    st = H.check_traced(cache, pp, inst, rot, rows, kappa, lens=inst.seq_lens, sink=4, window=W,
+                        bits=4)
+    exp = H.expected(inst, rot, pp, window=W, kappa=kappa, bits=4)
+    H.compare_pools(cache, exp)
+    H.report(f"int4 prefill[{wl.name},{lens},misalign={misalign}]", **st)
+    # sixteen levels put four times as many decision boundaries in a group
+    assert st["straddling_groups"] <= max(2, 0.02 * st["groups"])
     assert H.status(cache) == 0
 
 
@@ -66,8 +77,7 @@ def test_int4_append_steps_match_prefill_definition():
         L.oscar_quantize_append(cache, H.bf16_tensor(kn), H.bf16_tensor(vn),
                                 t.from_numpy(cur.astype(np.int32)).to(H.DEV))
     exp = H.expected(inst, rot, pp, window=W, lens=lens1, kappa=H.kappa(wl.head_dim), bits=4)
-    diff, flagged = H.compare_pools(cache, exp)
-    assert diff <= flagged
+    H.compare_pools(cache, exp)
     assert H.status(cache) == 0
 
 
@@ -118,7 +128,7 @@ def test_int4_fused_step_equals_append_then_decode():
     B, hkv = len(lens0), wl.num_kv_heads
     q = H.bf16_tensor(inst.q)
     max_len = int(lens1.max())
-    ws = t.empty(L.oscar_decode_workspace_size(fused, B, max_len) // 4 + 64, dtype=t.float32,
+    ws = t.zeros(L.oscar_decode_workspace_size(fused, B, max_len) // 4 + 64, dtype=t.float32,
                  device=H.DEV)
     for st in range(steps):
         cur = lens0 + st + 1
@@ -140,6 +150,5 @@ def test_int4_fused_step_equals_append_then_decode():
     np.testing.assert_array_equal(f2, s2)
     np.testing.assert_array_equal(fb, sb)
     exp = H.expected(inst, rot, pp, window=W, lens=lens1, kappa=H.kappa(wl.head_dim), bits=4)
-    diff, flagged = H.compare_pools(fused, exp)
-    assert diff <= flagged
+    H.compare_pools(fused, exp)   # bytes outside flagged near-boundary entries are exact
     assert H.status(fused) == 0 and H.status(split) == 0

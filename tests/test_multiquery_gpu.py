@@ -30,7 +30,7 @@ def _run(cache, q_rows, lens, pos, max_len):
     lt = t.from_numpy(np.asarray(lens, np.int32)).to(H.DEV)
     pt = t.from_numpy(pos.astype(np.int32)).to(H.DEV)
     out = t.zeros(q_rows.shape, dtype=t.bfloat16, device=H.DEV)
-    ws = t.empty(L.oscar_multiquery_workspace_size(cache, B, M, max_len) // 4 + 64,
+    ws = t.zeros(L.oscar_multiquery_workspace_size(cache, B, M, max_len) // 4 + 64,
                  dtype=t.float32, device=H.DEV)
     L.oscar_multiquery_attention(cache, q, lt, pt, max_len, out, ws)
     t.cuda.synchronize()

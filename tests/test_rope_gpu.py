@@ -57,7 +57,7 @@ def test_rope_step_matches_oracle(wl, lens0, steps, W):
     B, hkv, G = len(lens0), wl.num_kv_heads, wl.gqa
     q = H.bf16_tensor(inst.q)
     max_len = int(lens1.max())
-    ws = t.empty(L.oscar_decode_workspace_size(cache, B, max_len) // 4 + 64, dtype=t.float32,
+    ws = t.zeros(L.oscar_decode_workspace_size(cache, B, max_len) // 4 + 64, dtype=t.float32,
                  device=H.DEV)
     for st in range(steps):
         cur = lens0 + st + 1
@@ -85,8 +85,7 @@ def test_rope_step_matches_oracle(wl, lens0, steps, W):
                                   hkv=hkv, int2_table=pp.int2_table, bf16_table=pp.bf16_table,
                                   num_int2_pages=pp.num_int2_pages, num_bf16_pages=pp.num_bf16_pages,
                                   kappa=H.kappa(wl.head_dim), tokens=old)
-    diff, flagged = H.compare_pools(cache, exp)
-    assert diff <= flagged
+    H.compare_pools(cache, exp)   # bytes outside flagged near-boundary entries are exact
     # the new keys: within one bf16 ulp of the oracle's rotated key
     new = {b: list(range(int(lens0[b]), int(lens1[b]))) for b in range(B)}
     expn = H.ocache.expected_pools(rinst.k, rinst.v, lens1, rot, sink=4, window=W, d=wl.head_dim,
