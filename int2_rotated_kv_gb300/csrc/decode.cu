@@ -147,7 +147,8 @@ struct SplitCfg {
   // query operands: q' as fp16 hi and lo fragments ([D/16][32] uint2 each),
   // then the zero-term operand (uint32 [32])
   static constexpr int kLps = kIds + kMaxCtaPages * 4;
-  static constexpr int kQOperands = 2 * (D / 16) * 32 * 8 + 32 * 4 + 16;
+  static constexpr int kQzOff = 2 * (D / 16) * 32 * 8;                 // zero-term operand, flags
+  static constexpr int kQOperands = kQzOff + 32 * 4 + 16;
   static constexpr int kLpsBytes = kMaxCtaPages * 4 > kQOperands ? kMaxCtaPages * 4 : kQOperands;
   static constexpr int kBars = (kLps + kLpsBytes + 15) / 16 * 16;    // u64 [warps][stages]
   static constexpr int kRingOff = kBars + kDWarps * 8 * 8;
@@ -614,6 +615,9 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
     constexpr bool kPrecise = decltype(precise_tag)::value;
     const float ks = p.scale_log2 * 16777216.f;   // codes are read as code * 2^-24
     const float pe = int2_pscale_log2(p.clip_v[h]);
+    // the merge divides the weight 2^pe out again: it finds pe in shared
+    // memory (qzs[33] is read once every warp has left the loop)
+    if (warp == 0 && lane == 0) qzs[33] = __float_as_uint(pe);
     // every column sees INT2 tokens in [tok_lo, tok_hi); column 2tig (2tig+1)
     // sees them below min(L - window, lim0 (lim1)), worked out where a page needs masking
     const int tok_lo = p.sink, tok_hi = min(L - p.window, cs.lim_lo);
@@ -965,8 +969,10 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
 
   // ---- warp result -> shared scratch (the ring is idle once every warp is here)
   float l0 = sm.l0, l1 = sm.l1;
-  // INT2 pages: every probability carried the weight 2^pe
-  const float unw = mode == 0 ? exp2f(-int2_pscale_log2(p.clip_v[h])) : 1.f;
+  // INT2 pages: every probability carried the weight 2^pe (staged with q')
+  const float unw =
+      mode == 0 ? exp2f(-__uint_as_float(reinterpret_cast<const uint32_t*>(smem + C::kLps + C::kQzOff)[33]))
+                : 1.f;
   if (mode == 0) {
     // INT2 pages: the probability sum sits on row NG of the zero-term accumulator
     l0 = __shfl_sync(0xffffffffu, zacc[0], NG * 4 + tig) * unw;
@@ -985,8 +991,11 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
     zz1[g] = __shfl_sync(0xffffffffu, zacc[1], g * 4 + tig);
   }
   __syncthreads();
+  // per warp: [8] max, [8] sum, then the output channel-major, [D][8], so that
+  // a lane's two columns are one 8-byte store (a warp's stores fill 256
+  // consecutive bytes: no bank conflicts)
   float* scr = reinterpret_cast<float*>(ring);
-  float* wm = scr + warp * (16 + 8 * D);   // [8] max, [8] sum, [8][D] output
+  float* wm = scr + warp * (16 + 8 * D);
   float* wl = wm + 8;
   float* wo = wm + 16;
   if (gid == 0) {
@@ -1005,10 +1014,8 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
       v0 = fmaf(v0, sc, za); v1 = fmaf(v1, sc, zb);
       v2 = fmaf(v2, sc * 0.0625f, za); v3 = fmaf(v3, sc * 0.0625f, zb);
     }
-    wo[(2 * tig) * D + c0] = v0;
-    wo[(2 * tig + 1) * D + c0] = v1;
-    wo[(2 * tig) * D + c1] = v2;
-    wo[(2 * tig + 1) * D + c1] = v3;
+    *reinterpret_cast<float2*>(wo + c0 * 8 + 2 * tig) = make_float2(v0, v1);
+    *reinterpret_cast<float2*>(wo + c1 * 8 + 2 * tig) = make_float2(v2, v3);
   }
   __syncthreads();
   // per-warp weights 2^(m_w - M) once, then a plain weighted sum per element
@@ -1024,11 +1031,16 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
     if (w == 0) gmax[g] = M;
   }
   __syncthreads();
-  for (int idx = tid; idx < (kPacked ? G * nrows : G) * D; idx += kDThreads) {
-    const int g = idx / D, ch = idx % D;
+  // element (column g, channel ch), g fastest: the reads follow the [D][8]
+  // order, and each warp's stores fill 32-byte runs of a few partial rows
+  const int gv = kPacked ? G * cs.nrows : G;              // columns in use (<= 8)
+  const int gsh = gv > 4 ? 3 : (gv > 2 ? 2 : (gv > 1 ? 1 : 0));
+  for (int idx = tid; idx < (D << gsh); idx += kDThreads) {
+    const int g = idx & ((1 << gsh) - 1), ch = idx >> gsh;
+    if (g >= gv) continue;
     float Os = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDWarps; ++w) Os = fmaf(esc[w * 8 + g], scr[w * (16 + 8 * D) + 16 + g * D + ch], Os);
+    for (int w = 0; w < kDWarps; ++w) Os = fmaf(esc[w * 8 + g], scr[w * (16 + 8 * D) + 16 + ch * 8 + g], Os);
     float* dst = p.part +
                  ((static_cast<size_t>(kPacked ? b + g / G : b) * p.hq + qh0 + (kPacked ? g % G : g)) *
                       p.n_splits + split) * (D + 2);
@@ -1050,7 +1062,11 @@ constexpr int kMaxSplits = 2048;
 // One CTA per (query head, KV head, sequence).  Warp 0 finds the global max
 // and the split weights w_s = 2^(m_s - M); all threads then sum the weighted
 // split outputs channel by channel (coalesced, many loads in flight), and the
-// INT2 part is rotated back once: out = (o_raw + o_rot R_V^T) / l.
+// INT2 part is rotated back once: out = (o_raw + o_rot R_V^T) / l.  For the
+// rotation each warp holds RPW rows of R_V (a lane VPL columns of each) and
+// reduces its RPW partial dot products across the lanes by halving: at every
+// exchange a lane keeps half of its rows and adds the partner's half, so RPW
+// sums take RPW - 1 + log2(32 / RPW) + 1 shuffles instead of 5 RPW.
 template <int D, bool kBf16Only>
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
   constexpr int RPW = D / 8;              // output rows per warp
@@ -1150,15 +1166,36 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
   if (kBf16Only) {
     if (tid < D) dst[tid] = __bfloat16_as_ushort(__float2bfloat16_rn(acc_raw[0][tid] * inv));
   } else {
+    static_assert(RPW == 16 || RPW == 8, "the halving below takes 16 or 8 rows per warp");
+    float a[RPW];
 #pragma unroll
     for (int k = 0; k < RPW; ++k) {
-      const int i = warp * RPW + k;
-      float a = 0.f;
+      a[k] = 0.f;
 #pragma unroll
-      for (int u = 0; u < VPL; ++u) a = fmaf(orot[lane * VPL + u], rv[k][u], a);
+      for (int u = 0; u < VPL; ++u) a[k] = fmaf(orot[lane * VPL + u], rv[k][u], a[k]);
+    }
+    // halving: with n rows left, the lane whose bit `off` is set keeps rows
+    // n/2 .. n-1 (its partner rows 0 .. n/2-1) and receives the partner's
+    // partial sums of them.  After the exchange at off, row k of the n/2 kept
+    // rows is row k + (bit ? n/2 : 0) of the n; in the end lane l holds row
+    // (l >> 1) of the warp's (16 rows) or row (l >> 2) (8 rows).
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-      if (lane == 0) dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn((acc_raw[0][i] + a) * inv));
+    for (int n = RPW, off = 16; n > 1; n >>= 1, off >>= 1) {
+      const bool up = (lane & off) != 0;
+#pragma unroll
+      for (int k = 0; k < n / 2; ++k) {
+        const float send = up ? a[k] : a[k + n / 2];
+        const float keep = up ? a[k + n / 2] : a[k];
+        a[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    constexpr int kRest = 32 / RPW;   // lanes still sharing a row: 2 or 4
+    float s = a[0];
+#pragma unroll
+    for (int off = 1; off < kRest; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((lane & (kRest - 1)) == 0) {
+      const int i = warp * RPW + lane / kRest;
+      dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn((acc_raw[0][i] + s) * inv));
     }
   }
 }
