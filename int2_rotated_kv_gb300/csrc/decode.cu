@@ -1059,26 +1059,36 @@ __global__ void __launch_bounds__(kDThreads, SplitCfg<D, kBf16Only, P>::kCtasPer
 
 constexpr int kMaxSplits = 2048;
 
-// One CTA per (query head, KV head, sequence).  Warp 0 finds the global max
-// and the split weights w_s = 2^(m_s - M); all threads then sum the weighted
-// split outputs channel by channel (coalesced, many loads in flight), and the
-// INT2 part is rotated back once: out = (o_raw + o_rot R_V^T) / l.  For the
-// rotation each warp holds RPW rows of R_V (a lane VPL columns of each) and
-// reduces its RPW partial dot products across the lanes by halving: at every
-// exchange a lane keeps half of its rows and adds the partner's half, so RPW
-// sums take RPW - 1 + log2(32 / RPW) + 1 shuffles instead of 5 RPW.
-template <int D, bool kBf16Only>
-__global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
+// One CTA per KV head h and (batch row, query head of h) pair, or, with
+// kMulti, per run of pairs: then the CTA loads its share of R_V once and merges
+// its pairs one after another (many rows per KV head).  Per pair, warp 0 finds the global max and the split weights w_s = 2^(m_s - M);
+// all threads then sum the weighted split outputs channel by channel
+// (coalesced, many loads in flight), and the INT2 part is rotated back once:
+// out = (o_raw + o_rot R_V^T) / l.  With kMulti the next pair's partials are
+// requested while the current pair is summed and rotated.  For the rotation each warp
+// holds RPW rows of R_V (a lane VPL columns of each) and reduces its RPW
+// partial dot products across the lanes by halving: at every exchange a lane
+// keeps half of its rows and adds the partner's half, so RPW sums take
+// RPW - 1 + log2(32 / RPW) + 1 shuffles instead of 5 RPW.
+template <int D, bool kBf16Only, bool kMulti>
+__global__ void __launch_bounds__(256, kBf16Only ? 4 : 2) combine_kernel(const DecodeParams p) {
   constexpr int RPW = D / 8;              // output rows per warp
   constexpr int VPL = D / 32;             // R_V entries per lane per row
   constexpr int SG = 256 / D;             // split groups summed in parallel
+  constexpr int MAXR = 24;                // split outputs a thread holds in registers
   __shared__ float wsplit[kMaxSplits];
   __shared__ float acc_rot[SG][D];
   __shared__ float acc_raw[SG][D];
   __shared__ float orot[D];
-  __shared__ float lsum;
-  const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  __shared__ float lsum[2];               // by pair parity (read after the next pair began)
+  const int h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  // this CTA's pairs [q0, q1): pair q is query head h * G + q % G of row q / G
+  const int npairs = p.batch * p.G;
+  const int q0 = kMulti ? static_cast<int>(static_cast<int64_t>(blockIdx.x) * npairs / gridDim.x)
+                        : static_cast<int>(blockIdx.x);
+  const int q1 = kMulti ? static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * npairs / gridDim.x)
+                        : q0 + 1;
   float rv[kBf16Only ? 1 : RPW][VPL];
   if (!kBf16Only) {   // R_V does not depend on the previous kernel
     const float* r = p.r_v + static_cast<size_t>(h) * D * D;
@@ -1091,113 +1101,133 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeParams p) {
   }
   pdl_wait();
   pdl_trigger();
+  if (q0 >= q1) return;
   const int ns = p.n_splits;
-  const float* base = p.part + (static_cast<size_t>(b) * p.hq + h * p.G + g) * ns * (D + 2);
-  // every load that does not need the weights is issued in the first round trip
-  constexpr int MAXR = 24;
+  const int n_rot = kBf16Only ? 0 : p.n_main;
   const int ch = tid % D, sg = tid / D;
-  float ov[MAXR];
-#pragma unroll
-  for (int r = 0; r < MAXR; ++r) {
-    const int sp = sg + r * SG;
-    ov[r] = sp < ns ? base[sp * (D + 2) + 2 + ch] : 0.f;
-  }
-  if (warp == 0) {
-    float mv[2], lv[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int sp = lane + 32 * r;
-      mv[r] = sp < ns ? base[sp * (D + 2)] : -INFINITY;
-      lv[r] = sp < ns ? base[sp * (D + 2) + 1] : 0.f;
-    }
-    float M = fmaxf(mv[0], mv[1]);
-    for (int sp = lane + 64; sp < ns; sp += 32) M = fmaxf(M, base[sp * (D + 2)]);
-    M = warp_max(M);
-    float Ls = 0.f;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int sp = lane + 32 * r;
-      if (sp < ns) {
-        const float w = (mv[r] == -INFINITY) ? 0.f : exp2f(mv[r] - M);
-        wsplit[sp] = w;
-        Ls = fmaf(w, lv[r], Ls);
-      }
-    }
-    for (int sp = lane + 64; sp < ns; sp += 32) {
-      const float ms = base[sp * (D + 2)];
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wsplit[sp] = w;
-      Ls = fmaf(w, base[sp * (D + 2) + 1], Ls);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    if (lane == 0) lsum = Ls;
-  }
-  __syncthreads();
-  {
-    float ar = 0.f, aw = 0.f;
-    const int n_rot = kBf16Only ? 0 : p.n_main;
+  auto part_of = [&](int q) {
+    return p.part + (static_cast<size_t>(q / p.G) * p.hq + h * p.G + q % p.G) * ns * (D + 2);
+  };
+  // every load of a pair that does not need its weights, in one round trip
+  float ov[MAXR], mv[2], lv[2];
+  auto request = [&](const float* base) {
 #pragma unroll
     for (int r = 0; r < MAXR; ++r) {
       const int sp = sg + r * SG;
-      if (sp < ns) {
-        const float v = wsplit[sp] * ov[r];
+      ov[r] = sp < ns ? base[sp * (D + 2) + 2 + ch] : 0.f;
+    }
+    if (warp == 0) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int sp = lane + 32 * r;
+        mv[r] = sp < ns ? base[sp * (D + 2)] : -INFINITY;
+        lv[r] = sp < ns ? base[sp * (D + 2) + 1] : 0.f;
+      }
+    }
+  };
+  request(part_of(q0));
+  for (int q = q0; q < q1; ++q) {
+    const float* base = part_of(q);
+    if (warp == 0) {
+      float M = fmaxf(mv[0], mv[1]);
+      for (int sp = lane + 64; sp < ns; sp += 32) M = fmaxf(M, base[sp * (D + 2)]);
+      M = warp_max(M);
+      float Ls = 0.f;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int sp = lane + 32 * r;
+        if (sp < ns) {
+          const float w = (mv[r] == -INFINITY) ? 0.f : exp2f(mv[r] - M);
+          wsplit[sp] = w;
+          Ls = fmaf(w, lv[r], Ls);
+        }
+      }
+      for (int sp = lane + 64; sp < ns; sp += 32) {
+        const float ms = base[sp * (D + 2)];
+        const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+        wsplit[sp] = w;
+        Ls = fmaf(w, base[sp * (D + 2) + 1], Ls);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      if (lane == 0) lsum[q & 1] = Ls;
+    }
+    __syncthreads();
+    {
+      float ar = 0.f, aw = 0.f;
+#pragma unroll
+      for (int r = 0; r < MAXR; ++r) {
+        const int sp = sg + r * SG;
+        if (sp < ns) {
+          const float v = wsplit[sp] * ov[r];
+          if (sp < n_rot) ar += v; else aw += v;
+        }
+      }
+      for (int sp = sg + MAXR * SG; sp < ns; sp += SG) {
+        const float v = wsplit[sp] * base[sp * (D + 2) + 2 + ch];
         if (sp < n_rot) ar += v; else aw += v;
       }
+      acc_rot[sg][ch] = ar;
+      acc_raw[sg][ch] = aw;
     }
-    for (int sp = sg + MAXR * SG; sp < ns; sp += SG) {
-      const float v = wsplit[sp] * base[sp * (D + 2) + 2 + ch];
-      if (sp < n_rot) ar += v; else aw += v;
+    if (kMulti && q + 1 < q1) request(part_of(q + 1));   // in flight while this pair finishes
+    __syncthreads();
+    if (tid < D) {
+      float ar = 0.f, aw = 0.f;
+#pragma unroll
+      for (int k = 0; k < SG; ++k) { ar += acc_rot[k][tid]; aw += acc_raw[k][tid]; }
+      orot[tid] = ar;
+      acc_raw[0][tid] = aw;
     }
-    acc_rot[sg][ch] = ar;
-    acc_raw[sg][ch] = aw;
-  }
-  __syncthreads();
-  if (tid < D) {
-    float ar = 0.f, aw = 0.f;
+    __syncthreads();
+    const float l = lsum[q & 1];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint16_t* dst = p.out + (static_cast<size_t>(q / p.G) * p.hq + h * p.G + q % p.G) * D;
+    if (kBf16Only) {
+      if (tid < D) dst[tid] = __bfloat16_as_ushort(__float2bfloat16_rn(acc_raw[0][tid] * inv));
+    } else {
+      static_assert(RPW == 16 || RPW == 8, "the halving below takes 16 or 8 rows per warp");
+      float a[RPW];
 #pragma unroll
-    for (int k = 0; k < SG; ++k) { ar += acc_rot[k][tid]; aw += acc_raw[k][tid]; }
-    orot[tid] = ar;
-    acc_raw[0][tid] = aw;
-  }
-  __syncthreads();
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  uint16_t* dst = p.out + (static_cast<size_t>(b) * p.hq + h * p.G + g) * D;
-  if (kBf16Only) {
-    if (tid < D) dst[tid] = __bfloat16_as_ushort(__float2bfloat16_rn(acc_raw[0][tid] * inv));
-  } else {
-    static_assert(RPW == 16 || RPW == 8, "the halving below takes 16 or 8 rows per warp");
-    float a[RPW];
+      for (int k = 0; k < RPW; ++k) {
+        a[k] = 0.f;
 #pragma unroll
-    for (int k = 0; k < RPW; ++k) {
-      a[k] = 0.f;
+        for (int u = 0; u < VPL; ++u) a[k] = fmaf(orot[lane * VPL + u], rv[k][u], a[k]);
+      }
+      // halving: with n rows left, the lane whose bit `off` is set keeps rows
+      // n/2 .. n-1 (its partner rows 0 .. n/2-1) and receives the partner's
+      // partial sums of them.  After the exchange at off, row k of the n/2 kept
+      // rows is row k + (bit ? n/2 : 0) of the n; in the end lane l holds row
+      // (l >> 1) of the warp's (16 rows) or row (l >> 2) (8 rows).
 #pragma unroll
-      for (int u = 0; u < VPL; ++u) a[k] = fmaf(orot[lane * VPL + u], rv[k][u], a[k]);
-    }
-    // halving: with n rows left, the lane whose bit `off` is set keeps rows
-    // n/2 .. n-1 (its partner rows 0 .. n/2-1) and receives the partner's
-    // partial sums of them.  After the exchange at off, row k of the n/2 kept
-    // rows is row k + (bit ? n/2 : 0) of the n; in the end lane l holds row
-    // (l >> 1) of the warp's (16 rows) or row (l >> 2) (8 rows).
+      for (int n = RPW, off = 16; n > 1; n >>= 1, off >>= 1) {
+        const bool up = (lane & off) != 0;
 #pragma unroll
-    for (int n = RPW, off = 16; n > 1; n >>= 1, off >>= 1) {
-      const bool up = (lane & off) != 0;
+        for (int k = 0; k < n / 2; ++k) {
+          const float send = up ? a[k] : a[k + n / 2];
+          const float keep = up ? a[k + n / 2] : a[k];
+          a[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      constexpr int kRest = 32 / RPW;   // lanes still sharing a row: 2 or 4
+      float s = a[0];
 #pragma unroll
-      for (int k = 0; k < n / 2; ++k) {
-        const float send = up ? a[k] : a[k + n / 2];
-        const float keep = up ? a[k + n / 2] : a[k];
-        a[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      for (int off = 1; off < kRest; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if ((lane & (kRest - 1)) == 0) {
+        const int i = warp * RPW + lane / kRest;
+        dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn((acc_raw[0][i] + s) * inv));
       }
     }
-    constexpr int kRest = 32 / RPW;   // lanes still sharing a row: 2 or 4
-    float s = a[0];
-#pragma unroll
-    for (int off = 1; off < kRest; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if ((lane & (kRest - 1)) == 0) {
-      const int i = warp * RPW + lane / kRest;
-      dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn((acc_raw[0][i] + s) * inv));
-    }
+    // the next pair rewrites acc_rot / acc_raw / orot only after its first
+    // barrier, which every warp reaches after finishing this pair
   }
+}
+
+// The combine's CTAs per KV head in one wave of resident CTAs (two per SM).
+// A head with more (row, query head) pairs than that takes the multi-pair
+// form (INT2 only: the BF16 merge has no R_V to share).
+inline int combine_wave_per_head(int hkv) {
+  return std::max(1, (2 * oscar_host::sm_count() + hkv - 1) / hkv);
 }
 
 // ------------------------------------------------------------------- host
@@ -1289,7 +1319,14 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
     e = launch_pdl(split_kernel<D, kBf16Only, P, kPacked>, sgrid, dim3(kDThreads), C::kBytes, st, p);
   }
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
-  e = launch_pdl(combine_kernel<D, kBf16Only>, dim3(p.G, p.hkv, p.batch), dim3(256), 0, st, p);
+  const int npairs = p.batch * p.G, wave = combine_wave_per_head(p.hkv);
+  bool multi = false;
+  if constexpr (!kBf16Only) multi = npairs > wave;
+  if constexpr (!kBf16Only) {
+    if (multi) e = launch_pdl(combine_kernel<D, false, true>, dim3(wave, p.hkv), dim3(256), 0, st, p);
+  }
+  if (!multi)
+    e = launch_pdl(combine_kernel<D, kBf16Only, false>, dim3(npairs, p.hkv), dim3(256), 0, st, p);
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
