@@ -391,12 +391,14 @@ oscar_status launch_quantize(const QuantParams& p, cudaStream_t st) {
 // and a warp handles one sequence (lane j = output channel 32*grp + j).
 constexpr int kAppendSeqs = 8;      // sequences per CTA: one per warp
 
-template <int D, int P>
+// kGroup4 (batches of eight or more sequences): a warp rotates four queries
+// per pass over the R slice.
+template <int D, int P, bool kGroup4>
 __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) {
   constexpr int NG = D / 32;
   using F = Fmt<D, P>;
   __shared__ __align__(16) float rs[D][32];          // R[:, 32*grp .. 32*grp + 31]
-  __shared__ __align__(16) float xs[kQThreads / 32][D];
+  __shared__ __align__(16) float xs[kQThreads / 32][kGroup4 ? 4 : 1][D];   // per warp
   __shared__ uint8_t cs[kQThreads / 32][32];
   __shared__ double inv_freq[D / 2];                 // rotary base^(-2i/D)
   const int grp = blockIdx.x % NG, chunk = blockIdx.x / NG;
@@ -420,49 +422,85 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
   const uint16_t* src = kv ? p.v_src : p.k_src;
   const int j = 32 * grp + lane;                       // this lane's channel
   if (kv == 0 && p.qrot) {
-    // the step's rotated query: one (sequence, query head) task per warp, lane j
-    // computing channel 32*grp + j
+    // the step's rotated query, (sequence, query head) tasks, lane j computing
+    // channel 32*grp + j
     const int64_t left = p.n_items - static_cast<int64_t>(chunk) * kAppendSeqs;
     const int n_seq = static_cast<int>(left < kAppendSeqs ? left : kAppendSeqs);
-    // task t runs on warp (t + n_seq) mod 8: warps 0 .. n_seq-1 also place a
-    // token each below, so with few sequences the two chains run side by side
+    const int n_tasks = n_seq * p.G;
     constexpr int kWarps = kQThreads / 32;
-    const int t0 = ((warp - n_seq) % kWarps + kWarps) % kWarps;
-    for (int task = t0; task < n_seq * p.G; task += kWarps) {
+    // the task's query (rotated to the new token's position with rotary
+    // embedding, rounded to bf16) into row
+    auto stage = [&](int task, float* row) {
       const int b = chunk * kAppendSeqs + task / p.G, g = task % p.G;
       const uint16_t* qg = p.q + (static_cast<int64_t>(b) * p.hq + h * p.G + g) * D;
       const int m = rope ? p.seq_lens[b] - 1 : 0;   // issued with the query loads, not after them
 #pragma unroll
-      for (int c = 0; c < NG; ++c) xs[warp][32 * c + lane] = bf16_to_float(qg[32 * c + lane]);
+      for (int c = 0; c < NG; ++c) row[32 * c + lane] = bf16_to_float(qg[32 * c + lane]);
       __syncwarp();
-      if (rope) {   // the query at the new token's position, rounded to bf16
+      if (rope) {
         float v[NG];
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
           const int jj = 32 * c + lane;
-          v[c] = rope_bf16<D>(xs[warp][jj], xs[warp][jj < D / 2 ? jj + D / 2 : jj - D / 2], jj, m,
-                              inv_freq);
+          v[c] = rope_bf16<D>(row[jj], row[jj < D / 2 ? jj + D / 2 : jj - D / 2], jj, m, inv_freq);
         }
         __syncwarp();
 #pragma unroll
-        for (int c = 0; c < NG; ++c) xs[warp][32 * c + lane] = v[c];
+        for (int c = 0; c < NG; ++c) row[32 * c + lane] = v[c];
         __syncwarp();
         if (p.qrope)   // this CTA's 32 channels of the rotated query, for the BF16 split
           p.qrope[(static_cast<int64_t>(b) * p.hq + h * p.G + g) * D + j] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(xs[warp][j]));
+              __bfloat16_as_ushort(__float2bfloat16_rn(row[j]));
       }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    };
+    auto store = [&](int task, float v) {
+      const int b = chunk * kAppendSeqs + task / p.G, g = task % p.G;
+      p.qrot[(static_cast<int64_t>(b) * p.hq + h * p.G + g) * D + j] = v;
+    };
+    if (kGroup4 && n_tasks >= 4 * kWarps) {
+      // many tasks: four per pass over the R slice, so each shared-memory read
+      // of R serves four dot products (each task's sum in the same order as below)
+      for (int t4 = 4 * warp; t4 < n_tasks; t4 += 4 * kWarps) {
+        const int nt = min(4, n_tasks - t4);
+        for (int t = 0; t < nt; ++t) stage(t4 + t, xs[warp][kGroup4 ? t : 0]);
+        float acc[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < D; i += 4) {
+          const float r0 = rs[i][lane], r1 = rs[i + 1][lane], r2 = rs[i + 2][lane],
+                      r3 = rs[i + 3][lane];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float4 xv = *reinterpret_cast<const float4*>(&xs[warp][kGroup4 ? t : 0][i]);
+            acc[t][0] = fmaf(xv.x, r0, acc[t][0]);
+            acc[t][1] = fmaf(xv.y, r1, acc[t][1]);
+            acc[t][2] = fmaf(xv.z, r2, acc[t][2]);
+            acc[t][3] = fmaf(xv.w, r3, acc[t][3]);
+          }
+        }
+        for (int t = 0; t < nt; ++t) store(t4 + t, (acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3]));
+        __syncwarp();
+      }
+    } else {
+      // few tasks: one per warp, task t on warp (t + n_seq) mod 8: warps
+      // 0 .. n_seq-1 also place a token each below, so with few sequences the
+      // two chains run side by side
+      const int t0 = ((warp - n_seq) % kWarps + kWarps) % kWarps;
+      for (int task = t0; task < n_tasks; task += kWarps) {
+        stage(task, xs[warp][0]);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-      for (int i = 0; i < D; i += 4) {
-        const float4 xv = *reinterpret_cast<const float4*>(&xs[warp][i]);
-        acc[0] = fmaf(xv.x, rs[i][lane], acc[0]);
-        acc[1] = fmaf(xv.y, rs[i + 1][lane], acc[1]);
-        acc[2] = fmaf(xv.z, rs[i + 2][lane], acc[2]);
-        acc[3] = fmaf(xv.w, rs[i + 3][lane], acc[3]);
+        for (int i = 0; i < D; i += 4) {
+          const float4 xv = *reinterpret_cast<const float4*>(&xs[warp][0][i]);
+          acc[0] = fmaf(xv.x, rs[i][lane], acc[0]);
+          acc[1] = fmaf(xv.y, rs[i + 1][lane], acc[1]);
+          acc[2] = fmaf(xv.z, rs[i + 2][lane], acc[2]);
+          acc[3] = fmaf(xv.w, rs[i + 3][lane], acc[3]);
+        }
+        store(task, (acc[0] + acc[1]) + (acc[2] + acc[3]));
+        __syncwarp();
       }
-      p.qrot[(static_cast<int64_t>(b) * p.hq + h * p.G + g) * D + j] =
-          (acc[0] + acc[1]) + (acc[2] + acc[3]);
-      __syncwarp();
     }
   }
   for (int u = warp; u < kAppendSeqs; u += kQThreads / 32) {
@@ -506,14 +544,14 @@ __global__ void __launch_bounds__(kQThreads) append_kernel(const QuantParams p) 
     for (int c = 0; c < NG; ++c) {
       const int jj = 32 * c + lane;
       const int e = kv ? 16 * D + bf16_value_elem(slot, jj) : bf16_key_elem(slot, jj);
-      xs[warp][jj] = bf16_to_float(sblk[e]);
+      xs[warp][0][jj] = bf16_to_float(sblk[e]);
     }
     __syncwarp();
     // y_j = sum_i x_i R[i][j], fp32, four partial chains over i
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int i = 0; i < D; i += 4) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[warp][i]);
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[warp][0][i]);
       acc[0] = fmaf(xv.x, rs[i][lane], acc[0]);
       acc[1] = fmaf(xv.y, rs[i + 1][lane], acc[1]);
       acc[2] = fmaf(xv.z, rs[i + 2][lane], acc[2]);
@@ -541,7 +579,11 @@ oscar_status launch_append_p(const QuantParams& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, append_kernel<D, P>, p) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  // the grouped form only where a CTA has many query rotations to share R with
+  const bool group4 = p.qrot && p.n_items >= kAppendSeqs;
+  const cudaError_t e = group4 ? cudaLaunchKernelEx(&cfg, append_kernel<D, P, true>, p)
+                               : cudaLaunchKernelEx(&cfg, append_kernel<D, P, false>, p);
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 template <int D>
