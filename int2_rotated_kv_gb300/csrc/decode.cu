@@ -1223,6 +1223,139 @@ __global__ void __launch_bounds__(256, kBf16Only ? 4 : 2) combine_kernel(const D
   }
 }
 
+// The combine for many (row, query head) pairs that each have few splits
+// (ns <= kRowsMaxSplits: large batches): one CTA per KV head h and run of
+// pairs keeps R_V^T in shared memory, and a warp merges kRowsPairs pairs at a
+// time entirely in registers.  Lane l owns channels and output rows
+// l*CPL .. l*CPL + CPL-1: it reads every split's max and sum (the same words
+// for all lanes), weighs its channels of each split output, and forms
+// out_i = (o_raw_i + sum_j o_rot_j R_V[i][j]) / l from row j of R_V^T (one
+// conflict-free vector read per j, shared by the warp's pairs) and o_rot_j
+// broadcast from the warp's shared row.
+constexpr int kRowsPairs = 2;
+constexpr int kRowsMaxSplits = 4;
+
+template <int D>
+constexpr int rows_smem_bytes() {
+  return (D * (D + 4) + kDWarps * kRowsPairs * D) * 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 2) combine_rows_kernel(const DecodeParams p) {
+  constexpr int CPL = D / 32;             // channels (and output rows) per lane
+  constexpr int RS = D + 4;               // row stride of R_V^T (spreads the transposing stores)
+  constexpr int TP = kRowsPairs;
+  constexpr int NSX = kRowsMaxSplits;
+  extern __shared__ __align__(16) float rsm[];
+  float* rt = rsm;                        // [D][RS]: rt[j][i] = R_V[i][j]
+  const int h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  float* orow = rsm + D * RS + warp * TP * D;   // this warp's o_rot rows [TP][D]
+  {   // R_V is a constant of the layer: staged before the wait
+    const float* r = p.r_v + static_cast<size_t>(h) * D * D;
+    for (int e = tid; e < D * D; e += 256) rt[(e % D) * RS + e / D] = r[e];
+  }
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  const int npairs = p.batch * p.G;
+  const int q0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * npairs / gridDim.x);
+  const int q1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * npairs / gridDim.x);
+  const int ns = p.n_splits, n_rot = p.n_main;
+  for (int qb = q0 + warp * TP; qb < q1; qb += kDWarps * TP) {
+    float ml[TP][NSX][2], ov[TP][NSX][CPL];
+    // every load of the warp's pairs in one round trip
+#pragma unroll
+    for (int t = 0; t < TP; ++t) {
+      const int q = qb + t < q1 ? qb + t : qb;   // a spare slot repeats the first pair
+      const float* base = p.part + (static_cast<size_t>(q / p.G) * p.hq + h * p.G + q % p.G) * ns * (D + 2);
+#pragma unroll
+      for (int sx = 0; sx < NSX; ++sx) {
+        if (sx < ns) {
+          const float* ps = base + sx * (D + 2);
+          ml[t][sx][0] = ps[0];
+          ml[t][sx][1] = ps[1];
+#pragma unroll
+          for (int c = 0; c < CPL; c += 2) {
+            const float2 v = *reinterpret_cast<const float2*>(ps + 2 + lane * CPL + c);
+            ov[t][sx][c] = v.x;
+            ov[t][sx][c + 1] = v.y;
+          }
+        } else {
+          ml[t][sx][0] = -INFINITY;
+          ml[t][sx][1] = 0.f;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) ov[t][sx][c] = 0.f;
+        }
+      }
+    }
+    float oraw[TP][CPL], inv[TP];
+#pragma unroll
+    for (int t = 0; t < TP; ++t) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int sx = 0; sx < NSX; ++sx) M = fmaxf(M, ml[t][sx][0]);
+      float L = 0.f, orot[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) orot[c] = oraw[t][c] = 0.f;
+#pragma unroll
+      for (int sx = 0; sx < NSX; ++sx) {
+        const float w = (ml[t][sx][0] == -INFINITY) ? 0.f : exp2f(ml[t][sx][0] - M);
+        L = fmaf(w, ml[t][sx][1], L);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          if (sx < n_rot) orot[c] = fmaf(w, ov[t][sx][c], orot[c]);
+          else oraw[t][c] = fmaf(w, ov[t][sx][c], oraw[t][c]);
+        }
+      }
+      inv[t] = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; c += 2)
+        *reinterpret_cast<float2*>(orow + t * D + lane * CPL + c) = make_float2(orot[c], orot[c + 1]);
+    }
+    __syncwarp();
+    float acc[TP][CPL];
+#pragma unroll
+    for (int t = 0; t < TP; ++t)
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[t][c] = 0.f;
+#pragma unroll 2
+    for (int j4 = 0; j4 < D; j4 += 4) {
+      float4 oj[TP];
+#pragma unroll
+      for (int t = 0; t < TP; ++t) oj[t] = *reinterpret_cast<const float4*>(orow + t * D + j4);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        float r[CPL];
+        if constexpr (CPL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(rt + (j4 + jj) * RS + lane * 4);
+          r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(rt + (j4 + jj) * RS + lane * 2);
+          r[0] = v.x; r[1] = v.y;
+        }
+#pragma unroll
+        for (int t = 0; t < TP; ++t) {
+          const float o = jj == 0 ? oj[t].x : jj == 1 ? oj[t].y : jj == 2 ? oj[t].z : oj[t].w;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acc[t][c] = fmaf(o, r[c], acc[t][c]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TP; ++t) {
+      const int q = qb + t;
+      if (q < q1) {
+        uint16_t* dst = p.out + (static_cast<size_t>(q / p.G) * p.hq + h * p.G + q % p.G) * D + lane * CPL;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+          dst[c] = __bfloat16_as_ushort(__float2bfloat16_rn((oraw[t][c] + acc[t][c]) * inv[t]));
+      }
+    }
+    __syncwarp();   // the o_rot rows are rewritten by the next pass
+  }
+}
+
 // The combine's CTAs per KV head in one wave of resident CTAs (two per SM).
 // A head with more (row, query head) pairs than that takes the multi-pair
 // form (INT2 only: the BF16 merge has no R_V to share).
@@ -1323,7 +1456,13 @@ oscar_status run_decode(const DecodeParams& p, const Plan& pl, cudaStream_t st) 
   bool multi = false;
   if constexpr (!kBf16Only) multi = npairs > wave;
   if constexpr (!kBf16Only) {
-    if (multi) e = launch_pdl(combine_kernel<D, false, true>, dim3(wave, p.hkv), dim3(256), 0, st, p);
+    if (multi && p.n_splits <= kRowsMaxSplits) {
+      if (!oscar_host::allow_smem(reinterpret_cast<const void*>(combine_rows_kernel<D>), rows_smem_bytes<D>()))
+        return OSCAR_ERR_CUDA;
+      e = launch_pdl(combine_rows_kernel<D>, dim3(wave, p.hkv), dim3(256), rows_smem_bytes<D>(), st, p);
+    } else if (multi) {
+      e = launch_pdl(combine_kernel<D, false, true>, dim3(wave, p.hkv), dim3(256), 0, st, p);
+    }
   }
   if (!multi)
     e = launch_pdl(combine_kernel<D, kBf16Only, false>, dim3(npairs, p.hkv), dim3(256), 0, st, p);

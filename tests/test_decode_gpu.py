@@ -37,6 +37,28 @@ def test_decode_matches_oracle(wl, lens, W):
     assert H.status(cache) == 0
 
 
+def _ragged(n, lo, hi, seed):
+    return [int(x) for x in np.random.default_rng(seed).integers(lo, hi, size=n)]
+
+
+@pytest.mark.parametrize("wl,lens,W", [
+    # more (row, query head) pairs per KV head than a wave of combine CTAs, two
+    # or three splits each: the row-parallel merge (d = 128, and d = 64 with one
+    # KV head)
+    (synth.QWEN3_8B_32K, _ragged(44, 150, 1300, 1), 128),
+    (synth.TINY, _ragged(80, 70, 700, 2), 64),
+    # many pairs with more splits each (G = 8, six sequences): the merge that
+    # runs the pairs of a CTA one after another
+    (synth.QWEN3_32B_128K, _ragged(6, 2500, 3500, 3), 128),
+])
+def test_many_pairs_per_kv_head(wl, lens, W):
+    inst, rot, cache, pp, out = _run(wl, lens, W, n_calib=256)
+    ref = H.attention_from_pools(cache, pp, inst.q, inst.seq_lens, rot, sink=4, window=W,
+                                 gqa=wl.gqa)
+    H.check_close(out, ref, f"{wl.name} {len(lens)} sequences")
+    assert H.status(cache) == 0
+
+
 @pytest.mark.parametrize("g", [1, 2, 16])
 def test_small_gqa_groups(g):
     wl = synth.Workload("g%d" % g, batch=2, num_q_heads=2 * g, num_kv_heads=2, head_dim=128,
