@@ -368,6 +368,9 @@ def time_steps(dec, steps, warmup, chunk=64, clocks=None, barrier=None):
         clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    # a spin kernel ahead of the start event keeps the stream busy while the
+    # host submits the graphs, so their launch latency is not device time
+    torch.cuda._sleep(2_000_000)
     e0.record()
     for _ in range(steps // chunk):
         g_full.replay()
@@ -402,6 +405,7 @@ def time_graph(dec, fn, steps, warmup, chunk=64):
     torch.cuda.synchronize()
     reps = max(1, steps // chunk)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(2_000_000)   # the stream stays busy while the replays are submitted
     e0.record()
     for _ in range(reps):
         g.replay()
