@@ -715,10 +715,13 @@ __device__ __forceinline__ void int2_pages(const DecodeParams& p, int b, int h, 
 
 // BF16 pages (the sink + recent split, or every page of the BF16 baseline):
 // raw q against bf16 keys and values in the same fragment-native order.
-// kSplitP: the probabilities enter p.V as a bf16 pair (p = hi + lo, two MMAs),
-// so the weights are exact to ~2^-17 instead of bf16's 2^-9.  Used for the
-// sink + recent split of the mixed cache, where a query row may see only a few
-// tokens (a row early in a chunk); the all-BF16 baseline keeps one MMA.
+// kSplitP: the probabilities enter p.V as a bf16 pair (p = hi + mid, two MMAs),
+// exact to ~2^-17 instead of bf16's 2^-9, and for layers with large values
+// (value clip above 32) as three pieces (a third MMA: ~2^-25), each piece the
+// bf16 rounding of what the earlier ones leave.  Used for the sink + recent
+// split of the mixed cache, where a query row may see only a few tokens (a row
+// early in a chunk) or the window may hold most of the weight; the all-BF16
+// baseline keeps one MMA.
 template <int D, int NS, bool kSplitP, bool kPacked>
 __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, int warp, int lane,
                                            const int* ids, const int* lps, int n, int L, int mode,
@@ -760,6 +763,9 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
     }
   }
   const float scale_log2 = p.scale_log2;
+  // the third piece of p only for layers with large values (the value clip
+  // beyond the INT2 loop's fast-path bound; a NaN clip takes it too)
+  const bool p3 = kSplitP && !(fabsf(p.clip_v[h]) <= kFastValueClip);
   float zdummy[4] = {0.f, 0.f, 0.f, 0.f};
   uint32_t phase = 0;
   int s = 0;
@@ -803,13 +809,26 @@ __device__ __forceinline__ void bf16_pages(const DecodeParams& p, int b, int h, 
         mma_bf16(o[mt], a.x, a.y, a.z, a.w, pb0, pb1);
       }
       if constexpr (kSplitP) {
-        // the part of p the bf16 rounding dropped
-        const uint32_t pl0 = movmatrix_trans(pack_bf162(pr[0] - bf16_lo_value(h01), pr[1] - bf16_hi_value(h01)));
-        const uint32_t pl1 = movmatrix_trans(pack_bf162(pr[2] - bf16_lo_value(h23), pr[3] - bf16_hi_value(h23)));
+        // the parts of p the bf16 roundings dropped (each residual exact in fp32)
+        const float e0 = pr[0] - bf16_lo_value(h01), e1 = pr[1] - bf16_hi_value(h01);
+        const float e2 = pr[2] - bf16_lo_value(h23), e3 = pr[3] - bf16_hi_value(h23);
+        const uint32_t m01 = pack_bf162(e0, e1), m23 = pack_bf162(e2, e3);
+        const uint32_t pm0 = movmatrix_trans(m01), pm1 = movmatrix_trans(m23);
 #pragma unroll
         for (int mt = 0; mt < NK; ++mt) {
           const uint4 a = vb[mt * 32 + lane];
-          mma_bf16(o[mt], a.x, a.y, a.z, a.w, pl0, pl1);
+          mma_bf16(o[mt], a.x, a.y, a.z, a.w, pm0, pm1);
+        }
+        if (p3) {
+          const uint32_t pl0 =
+              movmatrix_trans(pack_bf162(e0 - bf16_lo_value(m01), e1 - bf16_hi_value(m01)));
+          const uint32_t pl1 =
+              movmatrix_trans(pack_bf162(e2 - bf16_lo_value(m23), e3 - bf16_hi_value(m23)));
+#pragma unroll
+          for (int mt = 0; mt < NK; ++mt) {
+            const uint4 a = vb[mt * 32 + lane];
+            mma_bf16(o[mt], a.x, a.y, a.z, a.w, pl0, pl1);
+          }
         }
       }
     }

@@ -199,6 +199,10 @@ def bf16_half_ulp(x):
     return 2.0 ** (np.floor(np.log2(x)) - 8)
 
 
+# the last check_close's largest deviation beyond the bf16 rounding of ref
+LAST_CHECK = {}
+
+
 def check_close(got, ref, what=""):
     """Output parity: rel-L2 <= 5e-3 and, per element, |got - ref| <= 1e-2 plus
     half a bf16 ulp of ref (the output is stored in bf16; for |out| >= 4 the
@@ -208,6 +212,7 @@ def check_close(got, ref, what=""):
     err = float(dev.max())
     worst = float(excess.max())
     rel = attention.rel_l2(got, ref)
+    LAST_CHECK["excess"] = worst
     assert worst <= TOL_MAX_ABS and rel <= TOL_REL_L2, \
         f"{what}: max-abs {err:.3e} (beyond bf16 rounding {worst:.3e}), rel-L2 {rel:.3e}"
     return err, rel
