@@ -451,9 +451,9 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       const __half z16 = __float2half_rn(mn);
       const float sf = __half2float(s16), zf = __half2float(z16);
       const bool live = sf != 0.f;            // a zero scale gives code 0 everywhere
-      // approximate reciprocal (a few ulp): the quotient stays far inside the
-      // near-tie margin below of the correctly rounded one
-      const float inv = live ? __fdividef(1.0f, sf) : 0.f;
+      // approximate reciprocal (a few ulp), times 1/top: the quotient stays far
+      // inside the near-tie margin below of the correctly rounded one
+      const float inv_top = live ? __fdividef(1.0f, sf) * (1.0f / kMaxCode) : 0.f;
       const uint32_t sz = static_cast<uint32_t>(__half_as_ushort(s16)) |
                           (static_cast<uint32_t>(__half_as_ushort(z16)) << 16);
       uint32_t bytes[P][8];
@@ -462,24 +462,28 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
 #pragma unroll
         for (int b8 = 0; b8 < 8; ++b8) bytes[pl][b8] = 0u;
       // code = round-half-even of the quotient clamped to [0, top] (the same as
-      // clamping the rounded quotient): adding 1.5 * 2^23 rounds it to an
-      // integer held in the low mantissa bits.  A clamped quotient within
-      // 6.4e-5 of a half-integer flags the group for the correctly rounded
-      // division; at the clamp bounds both roundings give the same code.
+      // clamping the rounded quotient).  The clamp is the saturation of
+      // t = (y - z) / (s top) to [0, 1] (a free modifier of the multiply; it
+      // also turns a NaN into 0); top * t + 1.5 * 2^23 in one fused
+      // multiply-add rounds the quotient to an integer held in the low
+      // mantissa bits, and a second one gives its distance from that integer.
+      // A clamped quotient within 6.4e-5 of a half-integer flags the group for
+      // the correctly rounded division; at the clamp bounds both roundings
+      // give the same code.
       constexpr float kMagic = 12582912.0f;
-      bool near = false;
+      constexpr float kTop = static_cast<float>(kMaxCode);
+      float dev = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float qc = fminf(fmaxf(__fmul_rn(__fsub_rn(y[j], zf), inv), 0.f),
-                               static_cast<float>(kMaxCode));
-        const float m = __fadd_rn(qc, kMagic);
-        near |= fabsf(__fsub_rn(qc, __fsub_rn(m, kMagic))) > 0.5f - 6.4e-5f;
+        const float t = __saturatef(__fmul_rn(__fsub_rn(y[j], zf), inv_top));
+        const float m = __fmaf_rn(t, kTop, kMagic);
+        dev = fmaxf(dev, fabsf(__fmaf_rn(t, kTop, -__fsub_rn(m, kMagic))));
         const uint32_t c = __float_as_uint(m);
         const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
 #pragma unroll
         for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
       }
-      if (live && near) {   // rare: the whole group again with the correctly rounded division
+      if (live && dev > 0.5f - 6.4e-5f) {   // rare: the whole group again with the correctly rounded division
 #pragma unroll
         for (int pl = 0; pl < P; ++pl)
 #pragma unroll

@@ -5,11 +5,15 @@ The kernel's fast path, per group of 32 rotated values y:
   - min and max over the raw values, then only those two clipped (clipping is
     monotone, so they equal the extremes of the clipped group);
   - s16 = fp16(fp32(mx - mn) / top), z16 = fp16(mn), as the definition;
-  - the quotient (y - z16) times a reciprocal of s16 that may be off by up to
-    two ulp, clamped to [0, top] and rounded by adding 1.5 * 2^23 (the code is
-    then the low mantissa bits);
+  - t = (y - z16) times (a reciprocal of s16 that may be off by up to two ulp,
+    times fp32(1/top)), saturated to [0, 1]; the quotient top * t is rounded by
+    one fused multiply-add with 1.5 * 2^23 (the code is then the low mantissa
+    bits), and a second fused multiply-add gives its distance from that integer;
   - the group goes to the correctly rounded division whenever a clamped
     quotient lies within 6.4e-5 of a half-integer.
+A fused multiply-add a * b + c of float32 values is restated as the float64
+product and sum rounded once to float32 (the product of a float32 t and a
+small integer top is exact in float64, and so is its sum with 1.5 * 2^23).
 Wherever a group is not flagged, every code must equal the definition's, for
 values inside and beyond the clip threshold alike."""
 import numpy as np
@@ -36,12 +40,15 @@ def fast_decide(y, clip, top, rng):
     # an approximate reciprocal: the correctly rounded one moved by up to two ulp
     steps = rng.integers(-2, 3, size=inv.shape).astype(np.int32)
     inv = np.where(live, (inv.view(np.int32) + steps).view(np.float32), np.float32(0.0))
-    q = ((y - zf[:, None]).astype(np.float32) * inv[:, None]).astype(np.float32)
-    qc = np.minimum(np.maximum(q, np.float32(0.0)), np.float32(top)).astype(np.float32)
-    m = (qc + MAGIC).astype(np.float32)
+    inv_top = (inv * np.float32(1.0 / top)).astype(np.float32)
+    q = ((y - zf[:, None]).astype(np.float32) * inv_top[:, None]).astype(np.float32)
+    t = np.minimum(np.maximum(q, np.float32(0.0)), np.float32(1.0)).astype(np.float32)
+    kt = t.astype(np.float64) * float(top)                    # exact
+    m = (kt + float(MAGIC)).astype(np.float32)                 # one rounding
     codes = (m.view(np.uint32) & np.uint32(0xF)).astype(np.uint8)
-    r = (m - MAGIC).astype(np.float32)
-    near = (np.abs((qc - r).astype(np.float32)) > MARGIN).any(axis=1) & live
+    r = (m - MAGIC).astype(np.float32)                         # exact
+    dist = (kt - r.astype(np.float64)).astype(np.float32)      # one rounding
+    near = (np.abs(dist) > MARGIN).any(axis=1) & live
     return codes, s16, z16, near
 
 
