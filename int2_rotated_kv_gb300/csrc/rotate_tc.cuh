@@ -473,15 +473,35 @@ __global__ void __launch_bounds__(TcSmem<D>::kThreads, 1)
       constexpr float kMagic = 12582912.0f;
       constexpr float kTop = static_cast<float>(kMaxCode);
       float dev = 0.f;
+      if constexpr (P == 1) {
+        // the codes as small integers in fp32 (r = rint(top t)); byte b holds
+        // the codes of values b, b + 8, b + 16, b + 24 at bit positions 0, 4,
+        // 2, 6, assembled as r0 + 16 r1 + 4 r2 + 64 r3 (exact) and turned into
+        // bits by one more 1.5 * 2^23 addition (the low byte is the value)
+        float r[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float t = __saturatef(__fmul_rn(__fsub_rn(y[j], zf), inv_top));
-        const float m = __fmaf_rn(t, kTop, kMagic);
-        dev = fmaxf(dev, fabsf(__fmaf_rn(t, kTop, -__fsub_rn(m, kMagic))));
-        const uint32_t c = __float_as_uint(m);
-        const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
+        for (int j = 0; j < 32; ++j) {
+          const float t = __saturatef(__fmul_rn(__fsub_rn(y[j], zf), inv_top));
+          r[j] = __fsub_rn(__fmaf_rn(t, kTop, kMagic), kMagic);
+          dev = fmaxf(dev, fabsf(__fmaf_rn(t, kTop, -r[j])));
+        }
 #pragma unroll
-        for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
+        for (int b8 = 0; b8 < 8; ++b8) {
+          const float v = __fmaf_rn(r[b8 + 24], 64.f,
+                                    __fmaf_rn(r[b8 + 16], 4.f, __fmaf_rn(r[b8 + 8], 16.f, r[b8])));
+          bytes[0][b8] = __float_as_uint(__fadd_rn(v, kMagic));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float t = __saturatef(__fmul_rn(__fsub_rn(y[j], zf), inv_top));
+          const float m = __fmaf_rn(t, kTop, kMagic);
+          dev = fmaxf(dev, fabsf(__fmaf_rn(t, kTop, -__fsub_rn(m, kMagic))));
+          const uint32_t c = __float_as_uint(m);
+          const int pos = 4 * ((j >> 3) & 1) + 2 * (j >> 4);
+#pragma unroll
+          for (int pl = 0; pl < P; ++pl) bytes[pl][j & 7] |= ((c >> (2 * (P - 1 - pl))) & 3u) << pos;
+        }
       }
       if (live && dev > 0.5f - 6.4e-5f) {   // rare: the whole group again with the correctly rounded division
 #pragma unroll
